@@ -1,0 +1,179 @@
+"""CPU oracle for the DSA indexer candidate-selection path -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
+reference leg may import this package.  The product path (the CUDA library and
+its Python binding) never imports, links or calls it.
+
+The arithmetic lives in ``dsa_oracle.c`` (plain single-threaded C, built here
+with gcc); this module only compiles it and marshals numpy arrays into it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(_HERE, "dsa_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+OK, EINVAL, ENOMEM = 0, -1, -2
+
+
+def compile_oracle(src: str, out: str) -> str:
+    """gcc -O2 a copy of the oracle source into a shared library at `out`."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    tmp = out + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, src],
+                   check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    if (force or not os.path.exists(_LIB_PATH)
+            or os.path.getmtime(_LIB_PATH) < os.path.getmtime(SOURCE)):
+        compile_oracle(SOURCE, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _bind(path: str):
+    L = ctypes.CDLL(path)
+    i32, i64, vp = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    L.oracle_key.restype = ctypes.c_uint32
+    L.oracle_key.argtypes = [ctypes.c_float]
+    L.oracle_bounds.restype = None
+    L.oracle_bounds.argtypes = [i32, vp, vp, i32, i32, i32, vp, vp]
+    L.oracle_block_scores.restype = i64
+    L.oracle_block_scores.argtypes = [vp, i64, i64, i64, i64, i32, vp]
+    L.oracle_block_topk.restype = i32
+    L.oracle_block_topk.argtypes = [vp, i64, i32, vp]
+    L.oracle_pin.restype = i64
+    L.oracle_pin.argtypes = [i64, i64, i32]
+    L.oracle_mask.restype = ctypes.c_int
+    L.oracle_mask.argtypes = [vp, i64, i64, i64, i64, i32, vp, i32]
+    L.oracle_row_topk.restype = i32
+    L.oracle_row_topk.argtypes = [vp, i64, i64, i64, i64, i32, vp]
+    L.oracle_row.restype = ctypes.c_int
+    L.oracle_row.argtypes = [vp, i64, i64, i64, i64, i32, i32, i32, vp, vp]
+    L.oracle_run.restype = ctypes.c_int
+    L.oracle_run.argtypes = [vp, i32, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, i32,
+                             vp, vp]
+    return L
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            _lib = _bind(build())
+    return _lib
+
+
+class Oracle:
+    """numpy-level access to one compiled oracle library (the default one, or a
+    deliberately altered copy used by the mutation tests)."""
+
+    def __init__(self, path: str | None = None):
+        self.L = lib() if path is None else _bind(path)
+
+    # ---- single steps -------------------------------------------------
+    def key(self, x: float) -> int:
+        return int(self.L.oracle_key(float(x)))
+
+    def bounds(self, r, starts, ends, rep=1, causal=True):
+        s = ctypes.c_int64()
+        e = ctypes.c_int64()
+        st = None if starts is None else np.ascontiguousarray(starts, dtype=np.int32)
+        en = np.ascontiguousarray(ends, dtype=np.int32)
+        self.L.oracle_bounds(int(r), None if st is None else st.ctypes.data, en.ctypes.data,
+                             int(st is not None), int(rep), int(bool(causal)),
+                             ctypes.byref(s), ctypes.byref(e))
+        return s.value, e.value
+
+    def block_scores(self, row, width, s, e, B, col_stride=1):
+        row = np.ascontiguousarray(row, dtype=np.float32)
+        NB = -(-width // B)
+        S = np.zeros(max(NB, 1), dtype=np.uint32)
+        nb = self.L.oracle_block_scores(row.ctypes.data, width, col_stride, s, e, B,
+                                        S.ctypes.data)
+        return S[:NB], nb
+
+    def block_topk(self, S, Kb):
+        S = np.ascontiguousarray(S, dtype=np.uint32)
+        T = np.zeros(Kb, dtype=np.int32)
+        n = self.L.oracle_block_topk(S.ctypes.data, len(S), Kb, T.ctypes.data)
+        if n < 0:
+            raise MemoryError
+        return T
+
+    def pin(self, s, e, B):
+        return int(self.L.oracle_pin(s, e, B))
+
+    def mask(self, row, width, s, e, B, cand, col_stride=1):
+        """Masks `row` (float32, C-contiguous) in place."""
+        assert row.dtype == np.float32 and row.flags.c_contiguous
+        cand = np.ascontiguousarray(cand, dtype=np.int32)
+        rc = self.L.oracle_mask(row.ctypes.data, width, col_stride, s, e, B,
+                                cand.ctypes.data, len(cand))
+        if rc != OK:
+            raise RuntimeError(f"oracle_mask: {rc}")
+        return row
+
+    def row_topk(self, row, width, s, e, K, col_stride=1):
+        row = np.ascontiguousarray(row, dtype=np.float32)
+        out = np.zeros(K, dtype=np.int32)
+        n = self.L.oracle_row_topk(row.ctypes.data, width, col_stride, s, e, K,
+                                   out.ctypes.data)
+        if n < 0:
+            raise MemoryError
+        return out
+
+    # ---- whole path -----------------------------------------------------
+    def row(self, row, width, s, e, B, Kb, K, col_stride=1):
+        """The whole path on one row (masked in place); returns (cand, topk)."""
+        assert row.dtype == np.float32 and row.flags.c_contiguous
+        cand = np.zeros(Kb + 1, dtype=np.int32)
+        topk = np.zeros(K, dtype=np.int32)
+        rc = self.L.oracle_row(row.ctypes.data, width, col_stride, s, e, B, Kb, K,
+                               cand.ctypes.data, topk.ctypes.data)
+        if rc != OK:
+            raise RuntimeError(f"oracle_row: {rc}")
+        return cand, topk
+
+    def run(self, logits, starts, ends, *, width, block_size, block_topk, row_topk,
+            row_repeat=1, causal=True, col_stride=1, row_stride=None):
+        """The whole path on every row of `logits` ([rows, row_stride] float32,
+        masked in place).  Returns (cand [rows, Kb+1], topk [rows, K])."""
+        assert logits.dtype == np.float32 and logits.flags.c_contiguous
+        rows = logits.shape[0]
+        if row_stride is None:
+            row_stride = logits.shape[1]
+        st = None if starts is None else np.ascontiguousarray(starts, dtype=np.int32)
+        en = np.ascontiguousarray(ends, dtype=np.int32)
+        cand = np.zeros((rows, block_topk + 1), dtype=np.int32)
+        topk = np.zeros((rows, row_topk), dtype=np.int32)
+        rc = self.L.oracle_run(logits.ctypes.data, rows, width, row_stride, col_stride,
+                               None if st is None else st.ctypes.data, en.ctypes.data,
+                               int(st is not None), row_repeat, int(bool(causal)),
+                               block_size, block_topk, row_topk, cand.ctypes.data,
+                               topk.ctypes.data)
+        if rc != OK:
+            raise RuntimeError(f"oracle_run: {rc}")
+        return cand, topk
+
+
+_default = None
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle()
+    return _default

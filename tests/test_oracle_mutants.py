@@ -1,0 +1,80 @@
+"""Mutation tests: plausible one-line mistakes planted in a temporary copy of
+the oracle source must each make at least one pin fail.  This shows the pins
+are not vacuous (the same check the mask kernel's authors ran with two
+kernel mutants, prhub report on vLLM PR #56628, implementation notes)."""
+import os
+
+import pytest
+
+import oracle
+from tests import test_oracle_pins as pins
+from tests.common import load_golden
+
+# (name, exact text in dsa_oracle.c, replacement)
+MUTANTS = [
+    ("key_keeps_negative_bits", "(u & 0x80000000u) ? ~u : (u | 0x80000000u)",
+     "(u & 0x80000000u) ? u : (u | 0x80000000u)"),
+    ("tie_to_higher_index", "return x->idx < y->idx ? -1 : 1;", "return x->idx > y->idx ? -1 : 1;"),
+    ("keys_ascending", "return x->key > y->key ? -1 : 1;", "return x->key < y->key ? -1 : 1;"),
+    ("block_max_reads_tail", "int64_t c1 = c0 + B < ec ? c0 + B : ec;",
+     "int64_t c1 = c0 + B < W ? c0 + B : W;"),
+    ("pin_from_clamped_end", "c[Kb] = (int32_t)oracle_pin(s, e, B);",
+     "c[Kb] = (int32_t)oracle_pin(s, e < W ? e : W, B);"),
+    ("edge_dropped", "edge = 1; /* clamped to the last column */", "edge = 0;"),
+    ("mask_full_width", "for (int64_t c = 0; c < ec; ++c) {\n    int keep = 0;",
+     "for (int64_t c = 0; c < W; ++c) {\n    int keep = 0;"),
+    ("mask_spares_before_start", "    int keep = 0;\n    if (c >= s)",
+     "    int keep = c < s;\n    if (c >= s)"),
+    ("partial_block_dropped", "return (ec - s + B - 1) / B;", "return (ec - s) / B;"),
+    ("topk_unsorted", "qsort(cols, (size_t)take, sizeof(int64_t), ascending_i64);", ""),
+    ("block_topk_one_short", "int64_t take = NB < Kb ? NB : Kb;",
+     "int64_t take = NB < Kb ? NB : Kb - 1;"),
+    ("causal_offset_wrong", "if (causal) e = e - (rep - 1) + (r % rep);",
+     "if (causal) e = e + (r % rep);"),
+    ("edge_wrong_column", "(c == W - 1 && edge)", "(c == W - 2 && edge)"),
+    ("packed_column_ignores_start", "if (s + b * (int64_t)B < W)", "if (b * (int64_t)B < W)"),
+    ("row_topk_take_one_short", "int64_t take = L < K ? L : K;", "int64_t take = L < K ? L : K - 1;"),
+]
+
+
+def _pins_fail(orc) -> list:
+    failed = []
+    checks = [("golden:" + c["name"], lambda c=c: pins.test_hand_worked_rows(orc, c))
+              for c in load_golden()["cases"]]
+    checks += [
+        ("block_scores", lambda: pins.test_hand_worked_block_scores(orc)),
+        ("key_order", lambda: pins.test_key_is_total_order(orc)),
+        ("brute", lambda: pins.test_brute_force_tiny(orc, False)),
+        ("brute_exotic", lambda: pins.test_brute_force_tiny(orc, True)),
+        ("brute_repeat", lambda: pins.test_brute_force_row_repeat(orc)),
+        ("b1_reduction", lambda: pins.test_b1_reduces_to_stable_topk(orc)),
+        ("invariants", lambda: pins.test_invariants_and_idempotence_random(orc)),
+    ]
+    for name, fn in checks:
+        try:
+            fn()
+        except AssertionError:
+            failed.append(name)
+    return failed
+
+
+def test_mutant_table_matches_source():
+    src = open(oracle.SOURCE).read()
+    for name, find, _ in MUTANTS:
+        assert src.count(find) == 1, f"mutant {name}: its target text must occur once"
+
+
+@pytest.mark.parametrize("name,find,repl", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_each_mutant_is_caught(tmp_path, name, find, repl):
+    src = open(oracle.SOURCE).read()
+    assert src.count(find) == 1
+    mutated = tmp_path / f"{name}.c"
+    mutated.write_text(src.replace(find, repl))
+    so = oracle.compile_oracle(str(mutated), str(tmp_path / f"lib{name}.so"))
+    failed = _pins_fail(oracle.Oracle(so))
+    assert failed, f"mutant {name} passed every pin"
+
+
+def test_unmutated_copy_passes(tmp_path):
+    so = oracle.compile_oracle(oracle.SOURCE, str(tmp_path / "libcopy.so"))
+    assert _pins_fail(oracle.Oracle(so)) == []

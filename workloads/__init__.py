@@ -1,0 +1,255 @@
+"""Seeded synthetic workloads for the DSA indexer candidate-selection path.
+
+This module only generates inputs (logits and per-row bounds).  It holds none
+of the selection arithmetic, so both the CUDA path and the CPU oracle can be fed
+from it without sharing any of the method's code.
+
+The five workloads follow the shapes the vLLM pages discuss for DeepSeek-V4.1
+decode and prefill (vLLM PR #57459 "DSA candidate-block kernels walk each row's
+live context", Summary; prhub report on vLLM PR #56628, test section):
+
+  tiny          4 rows x 4096, ends U{1..4096}, B=8, Kb=32, K=64
+  decode_short  64 rows x 131072, ends log-uniform in [128, 2048]
+  decode_1m     96 rows (48 requests x next_n 2, row_repeat 2) x 2^20,
+                ends lognormal(median 600) clipped to [1, 16384]
+  prefill_1m    2048 causal rows x 2^20, end = 1,046,273 + row,
+                64 planted spikes per row
+  ragged        128 rows x 262144 at column stride 2, starts U{0..512},
+                boundary ends, 1 % exact ties, 0.1 % -inf, B=16
+
+Every value is a pure function of (seed, stream, row, column) through a
+Philox4x32-10 counter generator, so single rows can be regenerated on their
+own for sampled checks at full size.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+from dataclasses import dataclass, field
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "synth.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "libsynth.so")
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile synth.c with gcc into workloads/_build/libsynth.so."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-fPIC", "-shared",
+                    "-pthread", "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib():
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            L = ctypes.CDLL(build())
+            L.synth_fill.restype = ctypes.c_int
+            L.synth_fill.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                ctypes.c_void_p, ctypes.c_int32, ctypes.c_uint32, ctypes.c_uint32,
+                ctypes.c_uint32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                ctypes.c_double, ctypes.c_int32]
+            L.synth_u32.restype = None
+            L.synth_u32.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                                    ctypes.c_int64, ctypes.c_void_p]
+            L.synth_philox4x32_10.restype = None
+            L.synth_philox4x32_10.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_void_p]
+            _lib = L
+    return _lib
+
+
+def philox4x32_10(counter, key) -> np.ndarray:
+    """One Philox4x32-10 block (exposed for known-answer tests)."""
+    c = np.asarray(counter, dtype=np.uint32)
+    k = np.asarray(key, dtype=np.uint32)
+    out = np.zeros(4, dtype=np.uint32)
+    lib().synth_philox4x32_10(c.ctypes.data, k.ctypes.data, out.ctypes.data)
+    return out
+
+
+def u32(seed: int, stream: int, row: int, n: int) -> np.ndarray:
+    out = np.zeros(max(n, 0), dtype=np.uint32)
+    if n > 0:
+        lib().synth_u32(seed, stream, row, n, out.ctypes.data)
+    return out
+
+
+def _unit(x: np.ndarray) -> np.ndarray:
+    return (x.astype(np.float64) + 0.5) * (1.0 / 4294967296.0)
+
+
+# Streams used for bounds (disjoint from the per-column streams in synth.c).
+_S_START = 101
+_S_END = 102
+_S_END_KIND = 103
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One synthetic configuration.  Sizes are in logits elements."""
+    name: str
+    rows: int
+    width: int
+    block_size: int
+    block_topk: int
+    row_topk: int
+    seed: int
+    row_repeat: int = 1
+    col_stride: int = 1
+    has_starts: bool = False
+    tie_ppm: int = 0
+    ninf_ppm: int = 0
+    spikes: int = 0
+    spike_base: float = 6.0
+    note: str = ""
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def row_stride(self) -> int:
+        return self.width * self.col_stride
+
+    @property
+    def n_bounds(self) -> int:
+        return -(-self.rows // self.row_repeat)
+
+    def with_(self, **kw) -> "Workload":
+        d = dict(self.__dict__)
+        d.update(kw)
+        return Workload(**d)
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", rows=4, width=4096, block_size=8, block_topk=32,
+                     row_topk=64, seed=0, note="ends U{1..4096}"),
+    "decode_short": Workload("decode_short", rows=64, width=131072, block_size=8,
+                             block_topk=256, row_topk=2048, seed=1,
+                             note="ends log-uniform in [128, 2048]"),
+    "decode_1m": Workload("decode_1m", rows=96, width=1 << 20, block_size=8,
+                          block_topk=256, row_topk=2048, seed=2, row_repeat=2,
+                          note="48 requests x next_n 2; per-request b ~ "
+                               "clip(round(lognormal(ln 600, 1)), 1, 16384); "
+                               "rows of a request end at b and b+1"),
+    "prefill_1m": Workload("prefill_1m", rows=2048, width=1 << 20, block_size=8,
+                           block_topk=256, row_topk=2048, seed=3, spikes=64,
+                           note="end = 1,046,273 + row; 64 spikes 6+|z| per row"),
+    "ragged": Workload("ragged", rows=128, width=262144, block_size=16,
+                       block_topk=256, row_topk=2048, seed=4, col_stride=2,
+                       has_starts=True, tie_ppm=10000, ninf_ppm=1000,
+                       note="starts U{0..512}; boundary and uniform ends; "
+                            "1% ties, 0.1% -inf; every 2nd float of [128, 524288]"),
+}
+
+
+def bounds(wl: Workload):
+    """Per-bound-entry (starts or None, ends) as int32 arrays of length n_bounds."""
+    n = wl.n_bounds
+    W, B = wl.width, wl.block_size
+    starts = None
+    if wl.name.startswith("tiny") or wl.extra.get("ends") == "uniform_full":
+        x = u32(wl.seed, _S_END, 0, n)
+        ends = 1 + (x.astype(np.int64) % W)
+    elif wl.name.startswith("decode_short"):
+        u = _unit(u32(wl.seed, _S_END, 0, n))
+        ends = np.rint(np.exp(math.log(128) + u * (math.log(2048) - math.log(128))))
+    elif wl.name.startswith("decode_1m"):
+        a = u32(wl.seed, _S_END, 0, 2 * n)
+        u1, u2 = _unit(a[0::2]), _unit(a[1::2])
+        z = np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)
+        b = np.clip(np.rint(np.exp(math.log(600.0) + 1.0 * z)), 1, 16384)
+        # the request's newest row ends one past its older row (next_n = 2)
+        ends = b + (wl.row_repeat - 1)
+    elif wl.name.startswith("prefill_1m"):
+        base = wl.extra.get("end_base", 1_046_273)
+        ends = base + np.arange(n, dtype=np.int64)
+    elif wl.name.startswith("ragged"):
+        s = u32(wl.seed, _S_START, 0, n).astype(np.int64) % 513
+        starts = s
+        special = [0, 1, 1023, 1024, 1025, W, W + 1, W + 7, W + B + 3]
+        kind = u32(wl.seed, _S_END_KIND, 0, 2 * n)
+        ends = np.zeros(n, dtype=np.int64)
+        for q in range(n):
+            if q < len(special):
+                ends[q] = special[q]
+                continue
+            k = int(kind[2 * q]) % 4
+            r = int(kind[2 * q + 1])
+            if k == 0:
+                ends[q] = special[r % 6]
+            elif k == 1:
+                ends[q] = special[6 + r % 3]
+            else:
+                lo = int(s[q])
+                ends[q] = lo + r % (W - lo + 1)
+    else:
+        raise KeyError(wl.name)
+    ends = np.asarray(ends, dtype=np.int64)
+    if starts is not None:
+        starts = np.asarray(starts, dtype=np.int32)
+    return starts, ends.astype(np.int32)
+
+
+def _live_ranges(wl: Workload, rows, starts, ends):
+    """[lo, hi) per requested row for tie sources and spike positions: the
+    bound entry's [start, min(end, width)) as the bounds generator laid it out
+    (workloads with spikes or ties have one bound entry per row)."""
+    rows = np.asarray(rows, dtype=np.int64)
+    q = rows // wl.row_repeat
+    e = ends[q].astype(np.int64)
+    s = starts[q].astype(np.int64) if starts is not None else np.zeros_like(e)
+    hi = np.minimum(e, wl.width)
+    lo = np.minimum(s, hi)
+    return lo.astype(np.int64), np.maximum(hi, lo).astype(np.int64)
+
+
+def fill_rows(wl: Workload, rows, out: np.ndarray, starts=None, ends=None,
+              nthreads: int | None = None) -> np.ndarray:
+    """Write the logits of absolute rows `rows` into `out` ([len(rows), row_stride]
+    float32, C-contiguous rows, may be a view of pinned memory)."""
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    if starts is None and ends is None:
+        starts, ends = bounds(wl)
+    assert out.dtype == np.float32 and out.ndim == 2 and out.shape[0] == len(rows)
+    assert out.shape[1] >= wl.row_stride and out.strides[1] == 4
+    lo, hi = _live_ranges(wl, rows, starts, ends)
+    lo = np.ascontiguousarray(lo)
+    hi = np.ascontiguousarray(hi)
+    if nthreads is None:
+        nthreads = os.cpu_count() or 1
+    rc = lib().synth_fill(out.ctypes.data, out.strides[0] // 4, wl.col_stride, wl.width,
+                          rows.ctypes.data, len(rows), wl.seed, wl.tie_ppm, wl.ninf_ppm,
+                          lo.ctypes.data, hi.ctypes.data, wl.spikes, wl.spike_base,
+                          nthreads)
+    if rc != 0:
+        raise ValueError("synth_fill rejected its arguments")
+    return out
+
+
+def make_rows(wl: Workload, rows, starts=None, ends=None) -> np.ndarray:
+    rows = list(rows)
+    out = np.empty((len(rows), wl.row_stride), dtype=np.float32)
+    return fill_rows(wl, rows, out, starts, ends)
+
+
+def make_all(wl: Workload, out: np.ndarray | None = None):
+    """(logits [rows, row_stride] float32, starts, ends) for the whole workload."""
+    starts, ends = bounds(wl)
+    if out is None:
+        out = np.empty((wl.rows, wl.row_stride), dtype=np.float32)
+    fill_rows(wl, range(wl.rows), out, starts, ends)
+    return out, starts, ends
