@@ -1,0 +1,440 @@
+#!/usr/bin/env python3
+"""Benchmark of the DSA indexer candidate-selection path on GB300.
+
+One step = one pass of the whole path (block scores, block top-k + pin, clamp,
+live-span mask, row top-k) over one batch: the fused dsa_select_topk launch on
+the 1M-context prefill chunk (2048 rows x 1,048,576 fp32 logits, 8 GiB, larger
+than L2, so no flush is needed between steps).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line on rank 0.  Under torchrun each rank processes its own
+replica batch (weak scaling, no data-path collective); timing is the max over
+ranks.  `--impl reference` times the CPU oracle instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wk  # noqa: E402
+
+KERNEL_SRC = os.path.join(ROOT, "sparse_attention_indexer_live_gb300", "csrc", "dsa_select.cu")
+PEAKS = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_NOTE = os.path.join(ROOT, "profiles", "select_topk_kernel_prefill_1m.md")
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "indexer select rows/s at W=1,048,576 (1M-context prefill chunk)"
+
+
+# ---------------------------------------------------------------------------
+# multi-rank plumbing (host only; the data path has no collective)
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return world, rank, local
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return world, rank
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_rows(rank: int, rows: int) -> np.ndarray:
+    """Row ids whose data rank `rank` generates: each rank gets its own rows of
+    the same shape (weak scaling), bounds shared."""
+    return np.arange(rows, dtype=np.int32) + rank * rows
+
+
+# ---------------------------------------------------------------------------
+# accounting
+
+def row_bounds(wl, starts, ends):
+    r = np.arange(wl.rows)
+    q = r // wl.row_repeat
+    e = ends[q].astype(np.int64) - (wl.row_repeat - 1) + (r % wl.row_repeat)
+    s = np.maximum(starts[q].astype(np.int64), 0) if starts is not None else np.zeros(wl.rows,
+                                                                                     np.int64)
+    return s, e
+
+
+def algorithmic_bytes(wl, starts, ends, cand) -> np.ndarray:
+    """Per-row minimum bytes of the path: read the live span when the values
+    matter (more live blocks than Kb), write -inf over every non-kept column of
+    [0, min(end, W)), write cand and topk, read the bounds."""
+    W, B, Kb, K = wl.width, wl.block_size, wl.block_topk, wl.row_topk
+    s, e = row_bounds(wl, starts, ends)
+    ec = np.minimum(e, W)
+    L = np.maximum(ec - s, 0)
+    nb = (L + B - 1) // B
+    out = np.zeros(wl.rows, dtype=np.int64)
+    for r in range(wl.rows):
+        c = cand[r].astype(np.int64)
+        c = c[c >= 0]
+        inside = s[r] + c * B < W
+        live = np.unique(c[inside & (c < nb[r])])
+        kept = int(np.minimum(B, ec[r] - (s[r] + live * B)).sum()) if len(live) else 0
+        edge = bool((~inside).any())
+        if edge and s[r] <= W - 1 < ec[r] and ((W - 1 - s[r]) // B) not in set(live.tolist()):
+            kept += 1
+        writes = max(int(ec[r]), 0) - kept
+        read = 4 * int(L[r]) if nb[r] > Kb else 0
+        out[r] = read + 4 * writes + 4 * (Kb + 1) + 4 * K + 8
+    return out
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, STREAM-style copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def kernel_source_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def committed_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    try:
+        txt = open(TRAFFIC_NOTE).read()
+    except OSError:
+        return None
+    vals = {}
+    for line in txt.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha256") != kernel_source_hash():
+        return None
+    try:
+        return int(vals["traffic_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# clocks
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.lines = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 10:
+                continue
+            try:
+                rows.append((t, float(p[2]), float(p[3]), p[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 and self.t1 and self.t0 <= r[0] <= self.t1]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "run (timed region shorter than the 100 ms sample period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "window": "no nvidia-smi samples"}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline / reference arm)
+
+def oracle_rows_per_s(wl, rows, starts, ends, threads):
+    """Time the oracle on the given rows (one row per task, `threads` host
+    threads; the oracle releases the GIL inside its C code)."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    orc = oracle.default()
+    data = wk.make_rows(wl, rows, starts, ends)
+    s, e = row_bounds(wl, starts, ends)
+
+    def one(i):
+        r = int(rows[i]) % wl.rows
+        orc.row(data[i], wl.width, int(s[r]), int(e[r]), wl.block_size, wl.block_topk,
+                wl.row_topk, col_stride=wl.col_stride)
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(one, range(len(rows))))
+    dt = time.perf_counter() - t0
+    return len(rows) / dt, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, wl):
+    world, rank = dist_init("gloo")
+    if rank != 0:
+        return
+    starts, ends = wk.bounds(wl)
+    cores = host_cores()
+    rng = np.random.default_rng(0)
+    per_step = cores
+    for _ in range(args.warmup):
+        oracle_rows_per_s(wl, rng.choice(wl.rows, per_step, replace=False), starts, ends, cores)
+    times = []
+    for _ in range(args.steps):
+        rows = rng.choice(wl.rows, per_step, replace=False)
+        _, dt = oracle_rows_per_s(wl, rows, starts, ends, cores)
+        times.append(dt)
+    total = sum(times)
+    value = per_step * args.steps / total
+    sample = (f"{per_step} random rows of the workload per step (one per host core), "
+              f"whole path per row, oracle as written")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": config_block(wl),
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(wl):
+    return {"workload": f"{wl.name}: {wl.rows} rows x {wl.width} fp32 logits, "
+                        f"B={wl.block_size}, block top-k={wl.block_topk} + newest-block pin, "
+                        f"row top-k={wl.row_topk}; {wl.note}",
+            "rows": wl.rows, "width": wl.width, "block_size": wl.block_size,
+            "block_topk": wl.block_topk, "row_topk": wl.row_topk,
+            "l2": "inputs (8 GiB) larger than the 129 MB L2; no flush between steps"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+def run_ours(args, wl):
+    import torch
+
+    import sparse_attention_indexer_live_gb300 as dsa
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist_init("nccl")
+    dev = torch.device("cuda", local)
+    dsa.build()
+    dsa.load()
+
+    starts, ends = wk.bounds(wl)
+    rows = replica_rows(rank, wl.rows)
+    host = torch.empty((wl.rows, wl.row_stride), dtype=torch.float32, pin_memory=True)
+    wk.fill_rows(wl, rows, host.numpy(), starts, ends)
+    logits = host.to(dev)
+    ends_h = torch.from_numpy(ends).pin_memory()
+    ends_d = ends_h.to(dev)
+    starts_d = None
+    cand = torch.empty((wl.rows, wl.block_topk + 1), dtype=torch.int32, device=dev)
+    topk = torch.empty((wl.rows, wl.row_topk), dtype=torch.int32, device=dev)
+    plan = dsa.dsa_select_init(device=local, rows=wl.rows, width=wl.width,
+                               block_size=wl.block_size, block_topk=wl.block_topk,
+                               row_topk=wl.row_topk, row_repeat=wl.row_repeat)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        dsa.dsa_select_topk(plan, logits, starts_d, ends_d, cand, topk, stream=stream)
+
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    clocks = ClockSampler(visible.split(",")[local].strip() if visible else str(local))
+    clocks.start()
+    # the first pass sees fresh logits; later passes run on the masked buffer,
+    # which the path leaves unchanged (same reads, same -inf writes, same output)
+    first = torch.cuda.Event(enable_timing=True)
+    first_end = torch.cuda.Event(enable_timing=True)
+    first.record(stream)
+    step()
+    first_end.record(stream)
+    torch.cuda.synchronize()
+    first_ms = first.elapsed_time(first_end)
+    cand_h = cand.cpu().numpy()
+    for _ in range(max(args.warmup - 1, 0)):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier()
+    torch.cuda.synchronize()
+    clocks.mark("t0")
+    evs[0].record(stream)
+    for i in range(args.steps):
+        step()
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    barrier()
+    total_ms = evs[0].elapsed_time(evs[-1])
+    launch_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(args.steps)]
+    total_ms = max_over_ranks(total_ms, dev)
+    clocks.stop()
+
+    # end to end through the public API: pinned host logits -> device, the
+    # fused call, cand + topk -> pinned host, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        cand_out = torch.empty(cand.shape, dtype=torch.int32, pin_memory=True)
+        topk_out = torch.empty(topk.shape, dtype=torch.int32, pin_memory=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            logits.copy_(host, non_blocking=True)
+            ends_d.copy_(ends_h, non_blocking=True)
+            step()
+            cand_out.copy_(cand, non_blocking=True)
+            topk_out.copy_(topk, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+        h2d = host.numel() * 4 + ends_h.numel() * 4
+        d2h = cand_out.numel() * 4 + topk_out.numel() * 4
+        e2e = {"value": wl.rows * world * args.e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps}
+
+    if rank != 0:
+        return
+    alg = algorithmic_bytes(wl, starts, ends, cand_h)
+    alg_launch = int(alg.sum())
+    avg_launch_s = statistics.mean(launch_ms) / 1e3
+    peak, peak_src = hbm_peak()
+    achieved = alg_launch / avg_launch_s / 1e9
+    traffic = committed_traffic()
+    value = wl.rows * world * args.steps / (total_ms / 1e3)
+    line = {
+        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded Philox4x32-10 N(0,1) logits with 64 planted +6 sigma "
+                "spikes per row)",
+        "config": config_block(wl),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "select_kernel<true> (fused dsa_select_topk)",
+                     "algorithmic_bytes_per_launch": alg_launch, "peak_source": peak_src,
+                     "avg_launch_ms": avg_launch_s * 1e3,
+                     "first_pass_ms": first_ms},
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+    }
+    if args.cpu_rows > 0:
+        cores = host_cores()
+        rng = np.random.default_rng(1)
+        sample = rng.choice(wl.rows, min(args.cpu_rows, wl.rows), replace=False)
+        v, dt = oracle_rows_per_s(wl, sample, starts, ends, cores)
+        line["cpu_baseline"] = {"value": v, "unit": "rows/s", "cores": min(cores, len(sample)),
+                                "kind": "oracle",
+                                "sample": f"{len(sample)} random rows of the workload, whole "
+                                          f"path per row, {dt:.1f} s wall"}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="prefill_1m", choices=sorted(wk.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-rows", type=int, default=96,
+                    help="rows of the oracle CPU baseline sample (0 = skip)")
+    args = ap.parse_args()
+    if args.warmup < 1:
+        ap.error("--warmup must be >= 1")
+    wl = wk.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

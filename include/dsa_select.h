@@ -1,0 +1,163 @@
+/*
+ * dsa_select.h -- C ABI of the GB300 (sm_103a) DeepSeek-sparse-attention
+ * indexer candidate-selection path.
+ *
+ * Given fp32 indexer logits [rows, W] and per-row [start, end) bounds, the
+ * path
+ *   1. scores every candidate block of B columns inside the row's live span
+ *      [start, min(end, W)) by the block's maximum,
+ *   2. takes the best Kb blocks (blocks past the span score -inf) and pins
+ *      the block holding the newest token (column end - 1, which may lie past
+ *      W),
+ *   3. clamps each candidate's packed column start + b*B: inside the buffer
+ *      it flags block b, past the buffer it sets the edge flag, which keeps
+ *      column W - 1 only,
+ *   4. writes -inf to every column of [0, min(end, W)) that is not kept and
+ *      never writes a column at or past min(end, W),
+ *   5. returns the best K column indices of the masked live span.
+ * Sources: vLLM PR #57459, "[Perf][Attention] DSA candidate-block kernels walk
+ * each row's live context", Summary; prhub report on vLLM PR #56628, "Stride
+ * the DSA decode candidate mask over the live context", key source excerpts
+ * (_mask_candidates_strided_kernel and _apply_candidate_mask_strided).
+ *
+ * Order: IEEE-754 totalOrder on the fp32 bit pattern (-NaN < -inf < ... <
+ * -0 < +0 < ... < +inf < +NaN); among equal values the lower index wins.  All
+ * results are exact (the path only compares and copies), so they match a
+ * plain CPU definition bit for bit.
+ *
+ * Conventions for every call below:
+ *   - Device pointers are CUDA device (or managed) addresses on the plan's
+ *     device; the caller owns and allocates all of them.  The library owns
+ *     only the host-side plan.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work: no host synchronisation, no allocation, no device
+ *     attribute query, so they can be captured in a CUDA graph.  The launch
+ *     grid depends on the plan (shapes) only; the work each CTA does follows
+ *     the bounds in device memory, so a captured graph stays valid when the
+ *     bounds change between replays.
+ *   - A plan with rows == 0 makes every call a no-op returning DSA_OK; its
+ *     pointers may then be NULL.
+ *   - Every call returns a status code (below) and never aborts.  A launch
+ *     failure is reported as DSA_ERR_CUDA; kernel faults surface, as usual
+ *     for CUDA, at the next synchronising call.
+ */
+#ifndef DSA_SELECT_H
+#define DSA_SELECT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t */
+
+enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* a NULL or misaligned pointer, a size out of range */
+  DSA_ERR_UNSUPPORTED = 2, /* valid, but beyond what this build supports (e.g. shared memory) */
+  DSA_ERR_CUDA = 3,        /* the CUDA runtime reported an error */
+  DSA_ERR_TIMEOUT = 4      /* a bounded device-side wait gave up */
+};
+
+/* Static shape of one call site.  All sizes count fp32 elements. */
+typedef struct dsa_select_cfg {
+  int32_t rows;          /* R >= 0 rows of logits                                    */
+  int32_t block_size;    /* B in [1, 4096]: columns per candidate block               */
+  int64_t width;         /* W in [1, 2^31 - 1]: columns per row (buffer width)        */
+  int64_t row_stride;    /* elements between rows; rows may not overlap               */
+  int64_t col_stride;    /* elements between columns (>= 1; 2 = packed pairs)         */
+  int32_t block_topk;    /* Kb in [1, 4096]: candidate blocks kept besides the pin    */
+  int32_t row_topk;      /* K in [1, 4096]: column indices returned per row           */
+  int32_t row_repeat;    /* rep >= 1: rows r read bound entry r / rep                 */
+  int32_t repeat_causal; /* 1: end of row r = ends[r/rep] - (rep-1) + r % rep
+                            0: every row of a group uses ends[r/rep] unchanged        */
+  int32_t has_starts;    /* 0: start = 0 for every row; 1: starts[] is given          */
+  int32_t reserved;      /* must be 0                                                 */
+} dsa_select_cfg;
+
+typedef struct dsa_select_plan dsa_select_plan;
+
+/* Launch geometry chosen by a plan (for tests and benchmarks). */
+typedef struct dsa_plan_desc {
+  int32_t threads;           /* threads per CTA                                       */
+  int32_t sm_count;          /* SMs on the plan's device                               */
+  int64_t nblocks;           /* NB = ceil(W / B)                                       */
+  int32_t vector_path;       /* 1: aligned rows stream with 128-bit accesses           */
+  int32_t stream_capacity;   /* entries of the streaming block top-k buffer            */
+  int32_t per_round;         /* most insertions one streaming round can make           */
+  int32_t candidate_capacity;/* (Kb + 1) * B + 1 candidate columns                     */
+  int64_t smem_select;       /* dynamic shared memory of the select kernel (bytes)     */
+  int64_t smem_topk_cand;    /* ... of the candidate-mode row top-k kernel             */
+  int64_t smem_topk_scan;    /* ... of the scan-mode row top-k kernel                  */
+  int32_t ctas_per_sm_select;/* resident select CTAs per SM                            */
+  int32_t grid_select;       /* CTAs per select launch                                 */
+} dsa_plan_desc;
+
+/*
+ * Build a plan for `cfg` on CUDA device `device`.  Validates the shape first
+ * (DSA_ERR_INVALID_ARG / DSA_ERR_UNSUPPORTED without touching CUDA), then
+ * reads the device's SM count and shared-memory limit and configures the
+ * kernels.  *plan receives a host object freed by dsa_select_destroy;
+ * *workspace_bytes (may be NULL) receives the device workspace every call of
+ * this plan needs (0 for this build: pass NULL).
+ */
+int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** plan,
+                    size_t* workspace_bytes);
+
+/* Free a plan (NULL is ignored).  No CUDA call is made. */
+void dsa_select_destroy(dsa_select_plan* plan);
+
+/* Copy out the plan's launch geometry. */
+int dsa_plan_describe(const dsa_select_plan* plan, dsa_plan_desc* out);
+
+/*
+ * Candidate selection and live-span mask (steps 1-4), in place.
+ *   logits  [rows, W] fp32, element (r, c) at logits[r*row_stride + c*col_stride];
+ *           4-byte aligned; rows whose start and column stride give 16-byte
+ *           alignment take the 128-bit path.  Read over each row's live span,
+ *           written with -inf over the non-kept columns of [0, min(end, W)).
+ *   starts  int32 [ceil(rows/rep)] (NULL iff cfg.has_starts == 0).  A negative
+ *           start is read as 0.
+ *   ends    int32 [ceil(rows/rep)]; may exceed W; end <= start is an empty row.
+ *   cand    int32 [rows, Kb + 1] output: the min(Kb, NB) chosen block ids in
+ *           ascending order, -1 padding, then the pin (-1 for an empty row).
+ *           Block b covers columns [start + b*B, start + (b+1)*B).
+ *   workspace  unused by this build (may be NULL).
+ */
+int dsa_candidate_select(const dsa_select_plan* plan, float* logits, const int32_t* starts,
+                         const int32_t* ends, int32_t* cand, void* workspace,
+                         struct CUstream_st* stream);
+
+/*
+ * Row top-k (step 5): the best K columns of [start, min(end, W)) by value,
+ * lower column on ties, as absolute column indices in ascending order with -1
+ * padding, into topk int32 [rows, K].
+ *   cand == NULL  scan mode: any logits; reads the whole live span.
+ *   cand != NULL  candidate mode: logits must be the output of
+ *                 dsa_candidate_select with the same bounds and this cand;
+ *                 reads only the candidate columns (plus, when fewer than K
+ *                 of them beat -inf, the first -inf columns of the span).
+ *                 Returns exactly what scan mode returns on those logits.
+ */
+int dsa_row_topk(const dsa_select_plan* plan, const float* logits, const int32_t* starts,
+                 const int32_t* ends, const int32_t* cand, int32_t* topk, void* workspace,
+                 struct CUstream_st* stream);
+
+/*
+ * Steps 1-5 fused in one launch: the result of dsa_candidate_select followed
+ * by dsa_row_topk in candidate mode, without re-reading the candidate list.
+ */
+int dsa_select_topk(const dsa_select_plan* plan, float* logits, const int32_t* starts,
+                    const int32_t* ends, int32_t* cand, int32_t* topk, void* workspace,
+                    struct CUstream_st* stream);
+
+/* Static description of a status code. */
+const char* dsa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_SELECT_H */

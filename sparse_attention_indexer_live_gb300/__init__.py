@@ -1,0 +1,16 @@
+"""GB300-native DeepSeek-sparse-attention indexer candidate selection.
+
+The work runs in hand-written sm_103a CUDA kernels behind a C ABI
+(include/dsa_select.h, built by ``build.build()``); this package is the thin
+Python binding over it.
+"""
+from .binding import (DSA_ERR_CUDA, DSA_ERR_INVALID_ARG, DSA_ERR_TIMEOUT, DSA_ERR_UNSUPPORTED,
+                      DSA_OK, DsaSelectError, EXPORTS, Plan, dsa_candidate_select,
+                      dsa_plan_desc, dsa_row_topk, dsa_select_cfg, dsa_select_init,
+                      dsa_select_topk, load, make_cfg, status_string)
+from .build import LIB_PATH, build
+
+__all__ = ["DSA_OK", "DSA_ERR_INVALID_ARG", "DSA_ERR_UNSUPPORTED", "DSA_ERR_CUDA",
+           "DSA_ERR_TIMEOUT", "DsaSelectError", "EXPORTS", "Plan", "dsa_select_cfg",
+           "dsa_plan_desc", "make_cfg", "dsa_select_init", "dsa_candidate_select",
+           "dsa_row_topk", "dsa_select_topk", "status_string", "load", "build", "LIB_PATH"]

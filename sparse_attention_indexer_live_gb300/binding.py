@@ -1,0 +1,200 @@
+"""Thin ctypes binding of libdsa_select.so (include/dsa_select.h).
+
+Argument marshalling only: torch tensors are turned into device pointers, the
+current CUDA stream is passed along, and a non-zero status becomes an
+exception.  Every step of the selection path runs in the library's kernels;
+there is no fallback of any kind -- if the library is missing, loading fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH
+
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED, DSA_ERR_CUDA, DSA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+
+
+class dsa_select_cfg(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("width", ctypes.c_int64), ("row_stride", ctypes.c_int64),
+                ("col_stride", ctypes.c_int64), ("block_topk", ctypes.c_int32),
+                ("row_topk", ctypes.c_int32), ("row_repeat", ctypes.c_int32),
+                ("repeat_causal", ctypes.c_int32), ("has_starts", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+class dsa_plan_desc(ctypes.Structure):
+    _fields_ = [("threads", ctypes.c_int32), ("sm_count", ctypes.c_int32),
+                ("nblocks", ctypes.c_int64), ("vector_path", ctypes.c_int32),
+                ("stream_capacity", ctypes.c_int32), ("per_round", ctypes.c_int32),
+                ("candidate_capacity", ctypes.c_int32), ("smem_select", ctypes.c_int64),
+                ("smem_topk_cand", ctypes.c_int64), ("smem_topk_scan", ctypes.c_int64),
+                ("ctas_per_sm_select", ctypes.c_int32), ("grid_select", ctypes.c_int32)]
+
+
+EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_candidate_select",
+           "dsa_row_topk", "dsa_select_topk", "dsa_status_string")
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DsaSelectError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def load(path: str | None = None):
+    """Load the CUDA library (raises OSError when it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or LIB_PATH
+            if not os.path.exists(p):
+                raise OSError(f"libdsa_select.so not built at {p}; run "
+                              "sparse_attention_indexer_live_gb300.build.build()")
+            L = ctypes.CDLL(p)
+            vp, i32 = ctypes.c_void_p, ctypes.c_int
+            L.dsa_select_init.restype = i32
+            L.dsa_select_init.argtypes = [ctypes.POINTER(dsa_select_cfg), i32,
+                                          ctypes.POINTER(vp), ctypes.POINTER(ctypes.c_size_t)]
+            L.dsa_select_destroy.restype = None
+            L.dsa_select_destroy.argtypes = [vp]
+            L.dsa_plan_describe.restype = i32
+            L.dsa_plan_describe.argtypes = [vp, ctypes.POINTER(dsa_plan_desc)]
+            L.dsa_candidate_select.restype = i32
+            L.dsa_candidate_select.argtypes = [vp, vp, vp, vp, vp, vp, vp]
+            L.dsa_row_topk.restype = i32
+            L.dsa_row_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+            L.dsa_select_topk.restype = i32
+            L.dsa_select_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+            L.dsa_status_string.restype = ctypes.c_char_p
+            L.dsa_status_string.argtypes = [i32]
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().dsa_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str):
+    if status != DSA_OK:
+        raise DsaSelectError(status, where)
+
+
+class Plan:
+    """A plan for one call-site shape (dsa_select_init)."""
+
+    def __init__(self, cfg: dsa_select_cfg, device: int):
+        L = load()
+        self._h = ctypes.c_void_p()
+        ws = ctypes.c_size_t(0)
+        _check(L.dsa_select_init(ctypes.byref(cfg), int(device), ctypes.byref(self._h),
+                                 ctypes.byref(ws)), "dsa_select_init")
+        self.cfg = cfg
+        self.device = int(device)
+        self.workspace_bytes = ws.value
+
+    @property
+    def handle(self):
+        return self._h
+
+    def describe(self) -> dict:
+        d = dsa_plan_desc()
+        _check(load().dsa_plan_describe(self._h, ctypes.byref(d)), "dsa_plan_describe")
+        return {name: getattr(d, name) for name, _ in d._fields_}
+
+    def close(self):
+        if self._h:
+            load().dsa_select_destroy(self._h)
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def make_cfg(*, rows, width, block_size, block_topk, row_topk, row_stride=None, col_stride=1,
+             row_repeat=1, repeat_causal=True, has_starts=False) -> dsa_select_cfg:
+    if row_stride is None:
+        row_stride = width * col_stride
+    return dsa_select_cfg(rows=rows, block_size=block_size, width=width, row_stride=row_stride,
+                          col_stride=col_stride, block_topk=block_topk, row_topk=row_topk,
+                          row_repeat=row_repeat, repeat_causal=int(bool(repeat_causal)),
+                          has_starts=int(bool(has_starts)), reserved=0)
+
+
+def dsa_select_init(cfg: dsa_select_cfg | None = None, device: int = 0, **shape) -> Plan:
+    """Plan for a shape given as a dsa_select_cfg or as keyword arguments
+    (rows, width, block_size, block_topk, row_topk, row_stride, col_stride,
+    row_repeat, repeat_causal, has_starts)."""
+    if cfg is None:
+        cfg = make_cfg(**shape)
+    return Plan(cfg, device)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_tensors(plan: Plan, logits, starts, ends, outs):
+    import torch
+    c = plan.cfg
+    assert logits.dtype == torch.float32 and logits.is_cuda, "logits: CUDA float32"
+    if logits.dim() == 2 and logits.shape[1] == c.width:
+        assert logits.shape[0] == c.rows, "logits rows"
+        assert (c.rows <= 1 or logits.stride(0) == c.row_stride) and \
+            logits.stride(1) == c.col_stride, "logits strides must match the plan"
+    else:
+        need = (c.rows - 1) * c.row_stride + (c.width - 1) * c.col_stride + 1 if c.rows else 0
+        assert logits.is_contiguous() and logits.numel() >= need, "logits storage too small"
+    nq = -(-c.rows // c.row_repeat)
+    assert ends.dtype == torch.int32 and ends.is_cuda and ends.is_contiguous() and \
+        ends.numel() >= nq, "ends: CUDA int32 [ceil(rows / row_repeat)]"
+    if c.has_starts:
+        assert starts is not None and starts.dtype == torch.int32 and starts.is_cuda and \
+            starts.is_contiguous() and starts.numel() >= nq, "starts"
+    else:
+        assert starts is None, "the plan was made without starts"
+    for name, t, cols in outs:
+        if t is not None:
+            assert t.dtype == torch.int32 and t.is_cuda and t.is_contiguous() and \
+                t.numel() >= c.rows * cols, f"{name}: CUDA int32 [rows, {cols}]"
+
+
+def dsa_candidate_select(plan: Plan, logits, starts, ends, cand, stream=None):
+    """Steps 1-4 in place on `logits`; cand [rows, Kb + 1] int32."""
+    _check_tensors(plan, logits, starts, ends, [("cand", cand, plan.cfg.block_topk + 1)])
+    _check(load().dsa_candidate_select(plan.handle, _ptr(logits), _ptr(starts), _ptr(ends),
+                                       _ptr(cand), None, _stream(stream)),
+           "dsa_candidate_select")
+
+
+def dsa_row_topk(plan: Plan, logits, starts, ends, cand, topk, stream=None):
+    """Step 5: topk [rows, K] int32; cand=None scans the live span."""
+    _check_tensors(plan, logits, starts, ends, [("cand", cand, plan.cfg.block_topk + 1),
+                                                ("topk", topk, plan.cfg.row_topk)])
+    _check(load().dsa_row_topk(plan.handle, _ptr(logits), _ptr(starts), _ptr(ends), _ptr(cand),
+                               _ptr(topk), None, _stream(stream)), "dsa_row_topk")
+
+
+def dsa_select_topk(plan: Plan, logits, starts, ends, cand, topk, stream=None):
+    """Steps 1-5 fused in one launch."""
+    _check_tensors(plan, logits, starts, ends, [("cand", cand, plan.cfg.block_topk + 1),
+                                                ("topk", topk, plan.cfg.row_topk)])
+    _check(load().dsa_select_topk(plan.handle, _ptr(logits), _ptr(starts), _ptr(ends),
+                                  _ptr(cand), _ptr(topk), None, _stream(stream)),
+           "dsa_select_topk")
