@@ -253,7 +253,7 @@ def run_reference(args, wl):
     starts, ends = wk.bounds(wl)
     cores = host_cores()
     rng = np.random.default_rng(0)
-    per_step = cores
+    per_step = min(cores, wl.rows)
     for _ in range(args.warmup):
         oracle_rows_per_s(wl, rng.choice(wl.rows, per_step, replace=False), starts, ends, cores)
     times = []
@@ -285,7 +285,8 @@ def config_block(wl):
                         f"row top-k={wl.row_topk}; {wl.note}",
             "rows": wl.rows, "width": wl.width, "block_size": wl.block_size,
             "block_topk": wl.block_topk, "row_topk": wl.row_topk,
-            "l2": "inputs (8 GiB) larger than the 129 MB L2; no flush between steps"}
+            "l2": f"inputs ({wl.rows * wl.row_stride * 4 / 2**30:.2f} GiB) larger than the "
+                  f"129 MB L2; no flush between steps"}
 
 
 # ---------------------------------------------------------------------------
@@ -305,7 +306,7 @@ def run_ours(args, wl):
     starts, ends = wk.bounds(wl)
     rows = replica_rows(rank, wl.rows)
     host = torch.empty((wl.rows, wl.row_stride), dtype=torch.float32, pin_memory=True)
-    wk.fill_rows(wl, rows, host.numpy(), starts, ends)
+    wk.fill_rows(wl, rows, host.numpy(), starts, ends, bound_rows=np.arange(wl.rows))
     logits = host.to(dev)
     ends_h = torch.from_numpy(ends).pin_memory()
     ends_d = ends_h.to(dev)
@@ -424,12 +425,16 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_1m", choices=sorted(wk.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--rows", type=int, default=None,
+                    help="override the workload's row count (smaller profiling cases)")
     ap.add_argument("--cpu-rows", type=int, default=96,
                     help="rows of the oracle CPU baseline sample (0 = skip)")
     args = ap.parse_args()
     if args.warmup < 1:
         ap.error("--warmup must be >= 1")
     wl = wk.WORKLOADS[args.workload]
+    if args.rows is not None:
+        wl = wl.with_(rows=args.rows)
     if args.impl == "reference":
         run_reference(args, wl)
     else:

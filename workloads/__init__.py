@@ -218,15 +218,19 @@ def _live_ranges(wl: Workload, rows, starts, ends):
 
 
 def fill_rows(wl: Workload, rows, out: np.ndarray, starts=None, ends=None,
-              nthreads: int | None = None) -> np.ndarray:
+              nthreads: int | None = None, bound_rows=None) -> np.ndarray:
     """Write the logits of absolute rows `rows` into `out` ([len(rows), row_stride]
-    float32, C-contiguous rows, may be a view of pinned memory)."""
+    float32, C-contiguous rows, may be a view of pinned memory).  `bound_rows`
+    (default: `rows`) names the row of the bounds each output row is laid out
+    for, so replica batches can draw fresh data rows for the same bounds."""
     rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
     if starts is None and ends is None:
         starts, ends = bounds(wl)
     assert out.dtype == np.float32 and out.ndim == 2 and out.shape[0] == len(rows)
     assert out.shape[1] >= wl.row_stride and out.strides[1] == 4
-    lo, hi = _live_ranges(wl, rows, starts, ends)
+    brows = rows if bound_rows is None else np.asarray(bound_rows, dtype=np.int64)
+    assert len(brows) == len(rows)
+    lo, hi = _live_ranges(wl, brows, starts, ends)
     lo = np.ascontiguousarray(lo)
     hi = np.ascontiguousarray(hi)
     if nthreads is None:
@@ -240,10 +244,10 @@ def fill_rows(wl: Workload, rows, out: np.ndarray, starts=None, ends=None,
     return out
 
 
-def make_rows(wl: Workload, rows, starts=None, ends=None) -> np.ndarray:
+def make_rows(wl: Workload, rows, starts=None, ends=None, bound_rows=None) -> np.ndarray:
     rows = list(rows)
     out = np.empty((len(rows), wl.row_stride), dtype=np.float32)
-    return fill_rows(wl, rows, out, starts, ends)
+    return fill_rows(wl, rows, out, starts, ends, bound_rows=bound_rows)
 
 
 def make_all(wl: Workload, out: np.ndarray | None = None):
