@@ -288,6 +288,104 @@ def config_block(wl):
             "l2": f"inputs ({wl.rows * wl.row_stride * 4 / 2**30:.2f} GiB) larger than the "
                   f"129 MB L2; no flush between steps"}
 
+# ---------------------------------------------------------------------------
+# supplementary measurements (not the bench metric): latency-bound shapes and
+# the scan-mode row top-k
+
+def _events(torch, n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def measure_extras(dsa, torch, dev, local, prefill):
+    out = {}
+    peak, _ = hbm_peak()
+    # 1M-width graph-captured decode: 96 rows, median end ~600
+    wl = wk.WORKLOADS["decode_1m"]
+    x, starts, ends = wk.make_all(wl)
+    logits = torch.from_numpy(x).to(dev)
+    del x
+    ends_d = torch.from_numpy(ends).to(dev)
+    cand = torch.empty((wl.rows, wl.block_topk + 1), dtype=torch.int32, device=dev)
+    topk = torch.empty((wl.rows, wl.row_topk), dtype=torch.int32, device=dev)
+    plan = dsa.dsa_select_init(device=local, rows=wl.rows, width=wl.width,
+                               block_size=wl.block_size, block_topk=wl.block_topk,
+                               row_topk=wl.row_topk, row_repeat=wl.row_repeat)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    dsa.dsa_select_topk(plan, logits, None, ends_d, cand, topk, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dsa.dsa_select_topk(plan, logits, None, ends_d, cand, topk, stream=s)
+    for _ in range(20):
+        g.replay()
+    torch.cuda.synchronize()
+    n = 500
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    for _ in range(n):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    warm_us = e0.elapsed_time(e1) * 1e3 / n
+    flush = torch.empty(64 << 20, dtype=torch.float32, device=dev)  # 256 MB > L2
+    ev = _events(torch, 2 * 50)
+    for i in range(50):
+        flush.fill_(float(i))
+        ev[2 * i].record()
+        g.replay()
+        ev[2 * i + 1].record()
+    torch.cuda.synchronize()
+    cold_us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(50))
+    alg = int(algorithmic_bytes(wl, starts, ends, cand.cpu().numpy()).sum())
+    full = wl.rows * wl.width * 4
+    out["decode_1m_graph"] = {
+        "rows": wl.rows, "us_per_replay_warm": warm_us, "us_per_replay_l2_flushed": cold_us,
+        "algorithmic_bytes": alg, "achieved_gbs_warm": alg / (warm_us * 1e-6) / 1e9,
+        "full_width_mask_bytes": full, "full_width_us_at_peak": full / (peak * 1e9) * 1e6}
+    del logits, flush, g
+    # one full 1M-column row (the pages' single-long-row case)
+    wl1 = wk.WORKLOADS["prefill_1m"].with_(rows=1)
+    x1 = wk.make_rows(wl1, [0], None, np.array([wl1.width], dtype=np.int32))
+    l1 = torch.from_numpy(x1).to(dev)
+    e1d = torch.tensor([wl1.width], dtype=torch.int32, device=dev)
+    c1 = torch.empty((1, wl1.block_topk + 1), dtype=torch.int32, device=dev)
+    t1 = torch.empty((1, wl1.row_topk), dtype=torch.int32, device=dev)
+    p1 = dsa.dsa_select_init(device=local, rows=1, width=wl1.width, block_size=wl1.block_size,
+                             block_topk=wl1.block_topk, row_topk=wl1.row_topk)
+    for _ in range(3):
+        dsa.dsa_select_topk(p1, l1, None, e1d, c1, t1)
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    for _ in range(20):
+        dsa.dsa_select_topk(p1, l1, None, e1d, c1, t1)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / 20
+    a1 = int(algorithmic_bytes(wl1, None, np.array([wl1.width], dtype=np.int32),
+                               c1.cpu().numpy()).sum())
+    out["single_row_1m"] = {"us_per_call": us, "achieved_gbs": a1 / (us * 1e-6) / 1e9,
+                            "ctas": p1.describe()["grid_select"]}
+    # scan-mode row top-k over the (masked) prefill logits
+    wlp, plan_p, logits_p, ends_p, topk_p = prefill
+    out_t = torch.empty_like(topk_p)
+    dsa.dsa_row_topk(plan_p, logits_p, None, ends_p, None, out_t)
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    for _ in range(3):
+        dsa.dsa_row_topk(plan_p, logits_p, None, ends_p, None, out_t)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / 3
+    _, e = row_bounds(wlp, None, ends_p.cpu().numpy())
+    L = np.minimum(e, wlp.width)
+    scan_alg = int((4 * L + 4 * wlp.row_topk + 8).sum())
+    out["scan_topk_prefill_1m"] = {
+        "ms_per_launch": ms, "rows_per_s": wlp.rows / (ms / 1e3),
+        "achieved_gbs": scan_alg / (ms / 1e3) / 1e9,
+        "matches_fused": bool(torch.equal(out_t, topk_p))}
+    return out
+
 
 # ---------------------------------------------------------------------------
 # our arm
@@ -405,6 +503,9 @@ def run_ours(args, wl):
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
     }
+    if args.extras:
+        line["extras"] = measure_extras(dsa, torch, dev, local,
+                                        (wl, plan, logits, ends_d, topk))
     if args.cpu_rows > 0:
         cores = host_cores()
         rng = np.random.default_rng(1)
@@ -425,9 +526,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_1m", choices=sorted(wk.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the supplementary decode / single-row / scan-mode timings")
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's row count (smaller profiling cases)")
-    ap.add_argument("--cpu-rows", type=int, default=96,
+    ap.add_argument("--cpu-rows", type=int, default=384,
                     help="rows of the oracle CPU baseline sample (0 = skip)")
     args = ap.parse_args()
     if args.warmup < 1:

@@ -74,7 +74,10 @@ typedef struct dsa_select_cfg {
   int32_t repeat_causal; /* 1: end of row r = ends[r/rep] - (rep-1) + r % rep
                             0: every row of a group uses ends[r/rep] unchanged        */
   int32_t has_starts;    /* 0: start = 0 for every row; 1: starts[] is given          */
-  int32_t reserved;      /* must be 0                                                 */
+  int32_t split;         /* CTAs per row in the select kernels: 0 = automatic (from
+                            rows, W and the SM count), else a power of two <= 16
+                            (a thread-block cluster per row when > 1); reduced when
+                            the device cannot schedule it                           */
 } dsa_select_cfg;
 
 typedef struct dsa_select_plan dsa_select_plan;
@@ -91,8 +94,10 @@ typedef struct dsa_plan_desc {
   int64_t smem_select;       /* dynamic shared memory of the select kernel (bytes)     */
   int64_t smem_topk_cand;    /* ... of the candidate-mode row top-k kernel             */
   int64_t smem_topk_scan;    /* ... of the scan-mode row top-k kernel                  */
-  int32_t ctas_per_sm_select;/* resident select CTAs per SM                            */
-  int32_t grid_select;       /* CTAs per select launch                                 */
+  int32_t ctas_per_sm_select;/* resident select CTAs per SM (unclustered kernel)        */
+  int32_t grid_select;       /* CTAs per select launch (rows * split)                  */
+  int32_t split;             /* CTAs per row chosen by the plan                        */
+  int32_t reserved;
 } dsa_plan_desc;
 
 /*

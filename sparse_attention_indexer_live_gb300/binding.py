@@ -22,7 +22,7 @@ class dsa_select_cfg(ctypes.Structure):
                 ("col_stride", ctypes.c_int64), ("block_topk", ctypes.c_int32),
                 ("row_topk", ctypes.c_int32), ("row_repeat", ctypes.c_int32),
                 ("repeat_causal", ctypes.c_int32), ("has_starts", ctypes.c_int32),
-                ("reserved", ctypes.c_int32)]
+                ("split", ctypes.c_int32)]
 
 
 class dsa_plan_desc(ctypes.Structure):
@@ -31,7 +31,8 @@ class dsa_plan_desc(ctypes.Structure):
                 ("stream_capacity", ctypes.c_int32), ("per_round", ctypes.c_int32),
                 ("candidate_capacity", ctypes.c_int32), ("smem_select", ctypes.c_int64),
                 ("smem_topk_cand", ctypes.c_int64), ("smem_topk_scan", ctypes.c_int64),
-                ("ctas_per_sm_select", ctypes.c_int32), ("grid_select", ctypes.c_int32)]
+                ("ctas_per_sm_select", ctypes.c_int32), ("grid_select", ctypes.c_int32),
+                ("split", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_candidate_select",
@@ -121,19 +122,19 @@ class Plan:
 
 
 def make_cfg(*, rows, width, block_size, block_topk, row_topk, row_stride=None, col_stride=1,
-             row_repeat=1, repeat_causal=True, has_starts=False) -> dsa_select_cfg:
+             row_repeat=1, repeat_causal=True, has_starts=False, split=0) -> dsa_select_cfg:
     if row_stride is None:
         row_stride = width * col_stride
     return dsa_select_cfg(rows=rows, block_size=block_size, width=width, row_stride=row_stride,
                           col_stride=col_stride, block_topk=block_topk, row_topk=row_topk,
                           row_repeat=row_repeat, repeat_causal=int(bool(repeat_causal)),
-                          has_starts=int(bool(has_starts)), reserved=0)
+                          has_starts=int(bool(has_starts)), split=int(split))
 
 
 def dsa_select_init(cfg: dsa_select_cfg | None = None, device: int = 0, **shape) -> Plan:
     """Plan for a shape given as a dsa_select_cfg or as keyword arguments
     (rows, width, block_size, block_topk, row_topk, row_stride, col_stride,
-    row_repeat, repeat_causal, has_starts)."""
+    row_repeat, repeat_causal, has_starts, split)."""
     if cfg is None:
         cfg = make_cfg(**shape)
     return Plan(cfg, device)

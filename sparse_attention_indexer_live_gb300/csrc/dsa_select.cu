@@ -26,6 +26,7 @@
 //
 // No device-side waits on other CTAs, no traps, no asserts.
 
+#include <cooperative_groups.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -47,6 +48,10 @@ constexpr int kBlocksPerThreadGeneric = 2;    // blocks per thread per round, sc
 constexpr int kMaxTopK = 4096;
 constexpr int kMaxBlockTopK = 4096;
 constexpr int kMaxBlockSize = 4096;
+constexpr int kMaxSplit = 16;                 // CTAs per row (thread-block cluster size)
+constexpr int32_t kMinBlocksPerCta = 1024;    // smallest share of a row's blocks worth a CTA
+
+namespace cg = cooperative_groups;
 
 struct Params {
   float* logits;
@@ -313,11 +318,12 @@ __device__ __forceinline__ int lower_bound_i32(const int32_t* a, int n, int32_t 
 }
 
 // ---------------------------------------------------------------------------
-// Step 1-2: streaming block top-Kb over the live span.  Leaves the best
-// candidates (a superset of the live top-Kb) in buf[0 .. sh.cnt).
+// Step 1-2: streaming block top-Kb over the live blocks [j0, j1) of the row.
+// Leaves the best candidates (a superset of the range's top-Kb) in
+// buf[0 .. sh.cnt).
 
-__device__ void stream_block_maxima(const Params& p, const float* rowp, const Row& R, uint64_t* buf,
-                                    uint64_t* keep, Shared& sh) {
+__device__ void stream_block_maxima(const Params& p, const float* rowp, const Row& R, int32_t j0,
+                                    int32_t j1, uint64_t* buf, uint64_t* keep, Shared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool vec = p.vec_log2g >= 0 && p.col_stride == 1 &&
                    (((uintptr_t)(rowp + R.s)) & 15u) == 0;
@@ -326,22 +332,24 @@ __device__ void stream_block_maxima(const Params& p, const float* rowp, const Ro
     const int g = 1 << g_log2;
     const float4* vp = reinterpret_cast<const float4*>(rowp + R.s);
     const int32_t L = R.L;
-    const int32_t nv = (L + 3) >> 2;
-    const int32_t nv_full = L >> 2;
+    const int32_t nv = (L + 3) >> 2;             // vectors touching the span
+    const int32_t nv_full = L >> 2;              // vectors inside it
+    const int32_t v_end = (int32_t)min((int64_t)j1 << g_log2, (int64_t)nv);
+    const int32_t v_full = min(v_end, nv_full);
     constexpr int32_t VR = kThreads * kVecPerThread;
     const float filler = __uint_as_float(kFillerBits);
-    for (int32_t rb = 0; rb < nv; rb += VR) {
+    for (int32_t rb = j0 << g_log2; rb < v_end; rb += VR) {
       if (sh.cnt > p.cap - p.prm) compact_best(buf, keep, p.Kb, p.cap, sh);
       const uint64_t tau = sh.tau;
       float4 x[kVecPerThread];
 #pragma unroll
       for (int u = 0; u < kVecPerThread; ++u) {
         const int32_t v = rb + (warp * kVecPerThread + u) * 32 + lane;
-        if (v < nv_full) {
+        if (v < v_full) {
           x[u] = __ldcs(vp + v);
         } else {
           x[u] = make_float4(filler, filler, filler, filler);
-          if (v < nv) {
+          if (v < v_end) {  // the span's last, partial vector
             const float* sp = rowp + R.s + 4 * (int64_t)v;
             const int rem = L - 4 * v;
             x[u].x = sp[0];
@@ -357,25 +365,24 @@ __device__ void stream_block_maxima(const Params& p, const float* rowp, const Ro
         const int32_t v = rb + (warp * kVecPerThread + u) * 32 + lane;
         const int32_t j = v >> g_log2;
         const uint64_t c = compose(m, (uint32_t)j);
-        const bool ins = ((lane & (g - 1)) == 0) && j < R.nb && c > tau;
+        const bool ins = ((lane & (g - 1)) == 0) && j < j1 && c > tau;
         warp_append(ins, c, buf, &sh.cnt, p.cap);
       }
       __syncthreads();
     }
   } else {
-    const int32_t nb = R.nb;
     const int64_t ec = R.s + R.L;
     const int64_t cs = p.col_stride;
     const int B = p.B;
     constexpr int32_t BR = kThreads * kBlocksPerThreadGeneric;
-    for (int32_t rb = 0; rb < nb; rb += BR) {
+    for (int32_t rb = j0; rb < j1; rb += BR) {
       if (sh.cnt > p.cap - p.prm) compact_best(buf, keep, p.Kb, p.cap, sh);
       const uint64_t tau = sh.tau;
 #pragma unroll
       for (int u = 0; u < kBlocksPerThreadGeneric; ++u) {
         const int32_t j = rb + u * kThreads + threadIdx.x;
         uint32_t m = 0;
-        const bool live = j < nb;
+        const bool live = j < j1;
         if (live) {
           const int64_t c0 = R.s + (int64_t)j * B;
           const int64_t c1 = c0 + B < ec ? c0 + B : ec;
@@ -397,21 +404,43 @@ __device__ void finish_block_topk(const Params& p, const Row& R, int r, uint64_t
                                   uint32_t* bitmap, Shared& sh) {
   const int Kb = p.Kb;
   if (sh.cnt > Kb) compact_best(buf, keep, Kb, p.cap, sh);
+  // buf now holds the live top-min(Kb, n_b), unordered
   int n = min(sh.cnt, p.cap - Kb);
-  const int64_t nvirt = p.nblocks - R.nb;
-  const int add = (int)(nvirt < Kb ? nvirt : Kb);
-  for (int i = threadIdx.x; i < add; i += kThreads) buf[n + i] = compose(kKeyNegInf, (uint32_t)(R.nb + i));
-  __syncthreads();
-  n += add;
   const int take = (int)(p.nblocks < Kb ? p.nblocks : Kb);
-  uint64_t X = 0;
-  if (n > take) X = select_kth(buf, n, take, sh);
-  for (int i = threadIdx.x; i < n; i += kThreads) {
-    const uint64_t c = buf[i];
-    if (c >= X) {
-      const uint32_t id = comp_index(c);
+  bool lo = false;
+  for (int i = threadIdx.x; i < n; i += kThreads) lo |= comp_key(buf[i]) < kKeyNegInf;
+  if (!__syncthreads_or(lo)) {
+    // No kept live block scores below -inf, so the -inf padding blocks rank
+    // right after all of them: the set is the live entries plus the first
+    // take - n padding ids (n_b, n_b + 1, ...).
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint32_t id = comp_index(buf[i]);
       atomicOr(&bitmap[id >> 5], 1u << (id & 31));
       if (R.s + (int64_t)id * p.B >= p.width) sh.edge = 1;
+    }
+    for (int i = threadIdx.x; i < take - n; i += kThreads) {
+      const int64_t id = (int64_t)R.nb + i;
+      atomicOr(&bitmap[id >> 5], 1u << (id & 31));
+      if (R.s + id * p.B >= p.width) sh.edge = 1;
+    }
+  } else {
+    // General case (a live maximum is -NaN): merge with up to Kb padding
+    // entries and select the best `take`.
+    const int64_t nvirt = p.nblocks - R.nb;
+    const int add = (int)(nvirt < Kb ? nvirt : Kb);
+    for (int i = threadIdx.x; i < add; i += kThreads)
+      buf[n + i] = compose(kKeyNegInf, (uint32_t)(R.nb + i));
+    __syncthreads();
+    n += add;
+    uint64_t X = 0;
+    if (n > take) X = select_kth(buf, n, take, sh);
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      const uint64_t c = buf[i];
+      if (c >= X) {
+        const uint32_t id = comp_index(c);
+        atomicOr(&bitmap[id >> 5], 1u << (id & 31));
+        if (R.s + (int64_t)id * p.B >= p.width) sh.edge = 1;
+      }
     }
   }
   __syncthreads();
@@ -435,37 +464,49 @@ __device__ void finish_block_topk(const Params& p, const Row& R, int r, uint64_t
   __syncthreads();
 }
 
-// Step 4: -inf over every non-kept column of [0, ecm); nothing at or past ecm.
-__device__ void write_mask(const Params& p, float* rowp, const Row& R, const uint32_t* bitmap, bool edge) {
+// Step 4 on columns [lo, hi) (hi <= ecm): -inf over every non-kept column;
+// nothing outside the range is written.
+__device__ void write_mask(const Params& p, float* rowp, const Row& R, const uint32_t* bitmap, bool edge,
+                           int64_t lo, int64_t hi) {
   const int64_t W = p.width;
-  const int32_t ecm = R.ecm;
   const int64_t s = R.s;
-  const bool edge_keep = edge && (W - 1) < ecm && (W - 1) >= s;
+  const bool edge_keep = edge && (W - 1) < R.ecm && (W - 1) >= s;
   const float ninf = __uint_as_float(kNegInfBits);
   const bool vec = p.vec_log2g >= 0 && p.col_stride == 1 && (((uintptr_t)rowp) & 15u) == 0 &&
                    (s & 3) == 0;
+  if (hi <= lo) return;
   if (vec) {
     const int log2B = p.log2B;
-    float4* vrow = reinterpret_cast<float4*>(rowp);
-    const float4 ninf4 = make_float4(ninf, ninf, ninf, ninf);
-    const int32_t nvec = ecm >> 2;
-    const int32_t edge_vec = (edge_keep && ((W & 3) == 0)) ? (int32_t)((W - 1) >> 2) : -1;
-#pragma unroll 4
-    for (int32_t v = threadIdx.x; v < nvec; v += kThreads) {
-      const int64_t c0 = (int64_t)v << 2;
+    // scalar head up to a 16-byte boundary, vectors, scalar tail
+    const int64_t vlo = (lo + 3) & ~(int64_t)3;
+    const int64_t vhi = hi & ~(int64_t)3;
+    for (int64_t c = lo + threadIdx.x; c < min(vlo, hi); c += kThreads) {
       bool kept = false;
-      if (c0 >= s) kept = bit_set(bitmap, (c0 - s) >> log2B);
-      if (!kept) {
-        if (v == edge_vec) {
-          rowp[c0] = ninf;
-          rowp[c0 + 1] = ninf;
-          rowp[c0 + 2] = ninf;
-        } else {
-          __stcs(vrow + v, ninf4);
+      if (c >= s) kept = bit_set(bitmap, (c - s) >> log2B) || (edge_keep && c == W - 1);
+      if (!kept) rowp[c] = ninf;
+    }
+    if (vhi > vlo) {
+      float4* vrow = reinterpret_cast<float4*>(rowp);
+      const float4 ninf4 = make_float4(ninf, ninf, ninf, ninf);
+      const int64_t edge_vec = (edge_keep && ((W & 3) == 0)) ? (W - 1) >> 2 : -1;
+      const int64_t v0 = vlo >> 2, v1 = vhi >> 2;
+#pragma unroll 4
+      for (int64_t v = v0 + threadIdx.x; v < v1; v += kThreads) {
+        const int64_t c0 = v << 2;
+        bool kept = false;
+        if (c0 >= s) kept = bit_set(bitmap, (c0 - s) >> log2B);
+        if (!kept) {
+          if (v == edge_vec) {
+            rowp[c0] = ninf;
+            rowp[c0 + 1] = ninf;
+            rowp[c0 + 2] = ninf;
+          } else {
+            __stcs(vrow + v, ninf4);
+          }
         }
       }
     }
-    for (int64_t c = ((int64_t)nvec << 2) + threadIdx.x; c < ecm; c += kThreads) {
+    for (int64_t c = max(vhi, vlo) + threadIdx.x; c < hi; c += kThreads) {
       bool kept = false;
       if (c >= s) kept = bit_set(bitmap, (c - s) >> log2B) || (edge_keep && c == W - 1);
       if (!kept) rowp[c] = ninf;
@@ -473,7 +514,7 @@ __device__ void write_mask(const Params& p, float* rowp, const Row& R, const uin
   } else {
     const int64_t cs = p.col_stride;
     const int B = p.B;
-    for (int64_t c = threadIdx.x; c < ecm; c += kThreads) {
+    for (int64_t c = lo + threadIdx.x; c < hi; c += kThreads) {
       bool kept = false;
       if (c >= s) kept = bit_set(bitmap, (c - s) / B) || (edge_keep && c == W - 1);
       if (!kept) rowp[c * cs] = ninf;
@@ -622,11 +663,24 @@ __device__ void row_topk_kept(const Params& p, const float* rowp, const Row& R, 
 // Dynamic shared memory of the select kernel:
 //   bitmap[bitmap_words] u32 | keep[Kb] u64 | region (max of the streaming
 //   buffer cap*8 and the candidate row top-k layout)
-template <bool kTopK>
+//
+// kCluster: a thread-block cluster of k CTAs owns one row.  Each CTA streams
+// an equal share of the row's live blocks into its own top-Kb; the leader
+// (rank 0) merges the k lists through distributed shared memory, finishes the
+// block top-k and builds the bitmap; every CTA copies the bitmap words of its
+// share back and masks its share; the leader takes the row top-k.  Only the
+// cluster's hardware barriers order these steps.
+template <bool kTopK, bool kCluster>
 __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ Shared sh;
-  const int r = blockIdx.x;
+  int r = blockIdx.x, rank = 0, k = 1;
+  if constexpr (kCluster) {
+    cg::cluster_group cl = cg::this_cluster();
+    rank = (int)cl.block_rank();
+    k = (int)cl.num_blocks();
+    r = blockIdx.x / k;
+  }
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(dyn);
   uint64_t* keep = reinterpret_cast<uint64_t*>(dyn + (((size_t)p.bitmap_words * 4 + 15) & ~(size_t)15));
   uint8_t* region = reinterpret_cast<uint8_t*>(keep + p.Kb);
@@ -642,12 +696,66 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   float* rowp = p.logits + (int64_t)r * p.row_stride;
   __syncthreads();
 
-  stream_block_maxima(p, rowp, R, buf, keep, sh);
+  // this CTA's share of the live blocks.  A row short enough for one CTA is
+  // left to the leader alone: every CTA of the cluster computes the same
+  // `parts` from the same bounds, so all of them skip the cluster barriers
+  // together and the other CTAs simply exit.
+  int32_t j0 = 0, j1 = R.nb;
+  int parts = 1;
+  if constexpr (kCluster) {
+    const int64_t want = ((int64_t)R.nb + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
+    parts = (int)(want < k ? (want > 0 ? want : 1) : k);
+    if (parts == 1 && rank != 0) return;
+    if (rank < parts) {
+      j0 = (int32_t)((int64_t)R.nb * rank / parts);
+      j1 = (int32_t)((int64_t)R.nb * (rank + 1) / parts);
+    } else {
+      j0 = j1 = 0;
+    }
+  }
+  const bool clustered = kCluster && parts > 1;
+  const int kk = clustered ? k : 1;
+  stream_block_maxima(p, rowp, R, j0, j1, buf, keep, sh);
   __syncthreads();
-  finish_block_topk(p, R, r, buf, keep, bitmap, sh);
+
+  if (clustered) {
+    cg::cluster_group cl = cg::this_cluster();
+    if (sh.cnt > p.Kb) compact_best(buf, keep, p.Kb, p.cap, sh);  // local top-Kb
+    cl.sync();  // every CTA's list is final
+    if (rank == 0) {
+      int n = sh.cnt;
+      for (int q = 1; q < k; ++q) {
+        const Shared* rsh = cl.map_shared_rank(&sh, (unsigned)q);
+        const uint64_t* rbuf = cl.map_shared_rank(buf, (unsigned)q);
+        const int cq = min(rsh->cnt, p.Kb);
+        for (int i = threadIdx.x; i < cq; i += kThreads) buf[n + i] = rbuf[i];
+        n += cq;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) sh.cnt = n;
+      __syncthreads();
+      finish_block_topk(p, R, r, buf, keep, bitmap, sh);
+    }
+    cl.sync();  // the leader's bitmap, edge flag and cand are final
+    if (rank != 0) {
+      const uint32_t* lbm = cl.map_shared_rank(bitmap, 0u);
+      for (int w = (j0 >> 5) + threadIdx.x; w < ((j1 + 31) >> 5); w += kThreads) bitmap[w] = lbm[w];
+      if (threadIdx.x == 0) sh.edge = cl.map_shared_rank(&sh, 0u)->edge;
+      __syncthreads();
+    }
+  } else {
+    finish_block_topk(p, R, r, buf, keep, bitmap, sh);
+  }
   const bool edge = sh.edge != 0;
-  write_mask(p, rowp, R, bitmap, edge);
-  if (kTopK) {
+  // mask: an even share of [0, min(s, ecm)) (column 0 .. start) and our blocks
+  const int64_t P = R.s < (int64_t)R.ecm ? R.s : (int64_t)R.ecm;
+  const int64_t plo = (P * rank / kk) & ~(int64_t)3;
+  const int64_t phi = rank + 1 == kk ? P : ((P * (rank + 1) / kk) & ~(int64_t)3);
+  write_mask(p, rowp, R, bitmap, edge, plo, phi);
+  const int64_t lhi = R.s + (int64_t)j1 * p.B;
+  write_mask(p, rowp, R, bitmap, edge, R.s + (int64_t)j0 * p.B, lhi < R.ecm ? lhi : (int64_t)R.ecm);
+  if (clustered) cg::this_cluster().sync();  // masks visible to the leader
+  if (kTopK && rank == 0) {
     __syncthreads();
     row_topk_kept(p, rowp, R, r, bitmap, edge, region, sh);
   }
@@ -680,18 +788,45 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cand_kernel(const Params p) 
   row_topk_kept(p, rowp, R, r, bitmap, sh.edge != 0, region, sh);
 }
 
-// Scan-mode row top-k: streaming top-K over the columns of the live span,
-// then an in-order pass that emits the chosen columns.
-// Dynamic shared memory: buf[scan_cap] u64 | keep[K] u64.
-__global__ void __launch_bounds__(kThreads, 1) topk_scan_kernel(const Params p) {
+// Ascending bitonic sort of a[0 .. n) in shared memory, n a power of two.
+__device__ void bitonic_sort_i32(int32_t* a, int n) {
+  for (int k = 2; k <= n; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const int32_t x = a[i], y = a[ixj];
+          if ((x > y) == ((i & k) == 0)) {
+            a[i] = y;
+            a[ixj] = x;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Scan-mode row top-k over the live span of any logits, in one pass.
+// The K best columns always lie in the K best 4-column groups ranked by the
+// group maximum (ties to the lower group): a column outside them would have
+// K better groups above it, each holding a distinct better column.  So the
+// kernel streams 128-bit group maxima through the same shared-memory
+// streaming top-K buffer as the block scores, sorts the chosen group ids,
+// gathers their columns in column order and radix-selects the K best.
+// Dynamic shared memory: region[max(scan_cap, 4K) u64] | keep[K] u64.
+constexpr int kScanGroup = 4;
+
+__global__ void __launch_bounds__(kThreads, 2) topk_scan_kernel(const Params p) {
   extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ Shared sh;
   const int r = blockIdx.x;
+  const int K = p.K;
   uint64_t* buf = reinterpret_cast<uint64_t*>(dyn);
-  uint64_t* keep = buf + p.scan_cap;
+  const int region_entries = p.scan_cap > K * kScanGroup ? p.scan_cap : K * kScanGroup;
+  uint64_t* keep = buf + region_entries;
   const Row R = load_row(p, r);
   const float* rowp = p.logits + (int64_t)r * p.row_stride;
-  const int K = p.K;
   int32_t* out = p.topk + (int64_t)r * K;
   const int64_t s = R.s;
   const int32_t L = R.L;
@@ -704,51 +839,46 @@ __global__ void __launch_bounds__(kThreads, 1) topk_scan_kernel(const Params p) 
     sh.tau = 0;
   }
   __syncthreads();
-  const int64_t cs = p.col_stride;
+  // 1. best K groups of kScanGroup columns by their maximum
+  Params q = p;
+  q.B = kScanGroup;
+  q.vec_log2g = p.col_stride == 1 ? 0 : -1;
+  q.Kb = K;
+  q.cap = p.scan_cap;
+  q.prm = p.scan_prm;
+  Row G = R;
+  G.nb = (L + kScanGroup - 1) / kScanGroup;
+  stream_block_maxima(q, rowp, G, 0, G.nb, buf, keep, sh);
+  __syncthreads();
+  if (sh.cnt > K) compact_best(buf, keep, K, q.cap, sh);
+  const int ng = min(sh.cnt, K);
+  // 2. their ids in ascending order (keep is free again: sort there)
+  int32_t* ids = reinterpret_cast<int32_t*>(keep);
+  int n2 = 1;
+  while (n2 < ng) n2 <<= 1;
+  for (int i = threadIdx.x; i < n2; i += kThreads) ids[i] = i < ng ? (int32_t)comp_index(buf[i]) : INT32_MAX;
+  __syncthreads();
+  bitonic_sort_i32(ids, n2);
+  // 3. gather the groups' columns in column order (buf is free again)
   const int64_t ec = s + L;
-  constexpr int kCols = 8;  // columns per thread per round
-  for (int64_t rb = s; rb < ec; rb += (int64_t)kThreads * kCols) {
-    if (sh.cnt > p.scan_cap - p.scan_prm) compact_best(buf, keep, K, p.scan_cap, sh);
-    const uint64_t tau = sh.tau;
-    uint32_t key[kCols];
-#pragma unroll
-    for (int u = 0; u < kCols; ++u) {
-      const int64_t c = rb + (int64_t)u * kThreads + threadIdx.x;
-      key[u] = c < ec ? order_key(__float_as_uint(__ldcg(rowp + c * cs))) : 0;
-    }
-#pragma unroll
-    for (int u = 0; u < kCols; ++u) {
-      const int64_t c = rb + (int64_t)u * kThreads + threadIdx.x;
-      const uint64_t v = compose(key[u], (uint32_t)c);
-      warp_append(c < ec && v > tau, v, buf, &sh.cnt, p.scan_cap);
-    }
-    __syncthreads();
+  const int64_t cs = p.col_stride;
+  const int ncand = ng * kScanGroup;
+  for (int t = threadIdx.x; t < ncand; t += kThreads) {
+    const int64_t c = s + (int64_t)ids[t / kScanGroup] * kScanGroup + (t % kScanGroup);
+    buf[t] = c < ec ? compose(order_key(__float_as_uint(__ldcg(rowp + c * cs))), (uint32_t)c) : 0;
   }
-  const int n = min(sh.cnt, p.scan_cap);
-  const uint64_t X = select_kth(buf, n, K, sh);
-  // emit chosen columns in order, 4 consecutive columns per thread per step
-  int written = 0;
-  for (int64_t base = s; base < ec && written < K; base += 4 * kThreads) {
-    const int64_t c0 = base + 4 * threadIdx.x;
-    uint32_t hits = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t c = c0 + k;
-      if (c < ec) {
-        const uint64_t v = compose(order_key(__float_as_uint(__ldcg(rowp + c * cs))), (uint32_t)c);
-        if (v >= X) hits |= 1u << k;
-      }
-    }
-    int tot;
-    int q = written + block_exclusive_scan(__popc(hits), &tot, sh);
-    while (hits) {
-      const int k = __ffs(hits) - 1;
-      if (q < K) out[q] = (int32_t)(c0 + k);
-      ++q;
-      hits &= hits - 1;
-    }
-    written += tot;
-  }
+  __syncthreads();
+  // 4. the K best candidates, emitted in column order
+  const uint64_t X = select_kth(buf, ncand, K, sh);
+  const int per = (ncand + kThreads - 1) / kThreads;
+  const int i0 = threadIdx.x * per;
+  const int i1 = min(i0 + per, ncand);
+  int cnt = 0;
+  for (int i = i0; i < i1; ++i) cnt += buf[i] != 0 && buf[i] >= X;
+  int total;
+  int pos = block_exclusive_scan(cnt, &total, sh);
+  for (int i = i0; i < i1; ++i)
+    if (buf[i] != 0 && buf[i] >= X && pos < K) out[pos++] = (int32_t)comp_index(buf[i]);
 }
 
 }  // namespace
@@ -760,6 +890,7 @@ struct dsa_select_plan {
   dsa_select_cfg cfg;
   int device;
   int sm_count;
+  int split;  // CTAs per row in the select kernels (cluster size; 1 = no cluster)
   Params base;
   size_t smem_select;
   size_t smem_topk_cand;
@@ -787,13 +918,90 @@ int validate(const dsa_select_cfg* c) {
   if (c->row_repeat < 1) return DSA_ERR_INVALID_ARG;
   if (c->has_starts != 0 && c->has_starts != 1) return DSA_ERR_INVALID_ARG;
   if (c->repeat_causal != 0 && c->repeat_causal != 1) return DSA_ERR_INVALID_ARG;
-  if (c->reserved != 0) return DSA_ERR_INVALID_ARG;
+  if (c->split < 0 || (c->split & (c->split - 1)) != 0) return DSA_ERR_INVALID_ARG;
   const int64_t row_span = (c->width - 1) * c->col_stride + 1;
   if (c->rows > 1 && c->row_stride < row_span) return DSA_ERR_INVALID_ARG;
   if (c->row_stride < 0) return DSA_ERR_INVALID_ARG;
-  if (c->block_size > kMaxBlockSize || c->block_topk > kMaxBlockTopK || c->row_topk > kMaxTopK)
+  if (c->block_size > kMaxBlockSize || c->block_topk > kMaxBlockTopK || c->row_topk > kMaxTopK ||
+      c->split > kMaxSplit)
     return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
+}
+
+struct Sizes {
+  int cap;
+  size_t select, cand, scan;
+};
+
+// Shared-memory sizes for a plan whose select kernel runs `split` CTAs per row
+// (the cluster leader's buffer must hold every CTA's top-Kb plus Kb padding).
+Sizes sizes_for(Params& P, int split) {
+  int cap = P.Kb + 2 * P.prm;
+  if (cap < 2 * P.Kb) cap = 2 * P.Kb;
+  if (cap < (split + 1) * P.Kb) cap = (split + 1) * P.Kb;
+  if (cap < 4096) cap = 4096;
+  P.cap = (cap + 255) & ~255;
+  const size_t bitmap_bytes = align16((size_t)P.bitmap_words * 4);
+  const size_t cand_layout = align16((size_t)P.cand_cap * 16 + (size_t)(P.Kb + 1) * 4 +
+                                     (size_t)(P.K > P.cand_cap ? P.K : P.cand_cap) * 4 +
+                                     (size_t)P.K * 4);
+  const size_t stream_bytes = (size_t)P.cap * 8;
+  const size_t region = stream_bytes > cand_layout ? stream_bytes : cand_layout;
+  Sizes z;
+  z.cap = P.cap;
+  z.select = bitmap_bytes + align16((size_t)P.Kb * 8) + region;
+  z.cand = bitmap_bytes + cand_layout;
+  const size_t scan_region = (size_t)(P.scan_cap > P.K * kScanGroup ? P.scan_cap : P.K * kScanGroup);
+  z.scan = scan_region * 8 + (size_t)P.K * 8;
+  return z;
+}
+
+template <bool kTopK>
+cudaError_t launch_select(const dsa_select_plan* plan, const Params& P, cudaStream_t stream) {
+  const int k = plan->split;
+  if (k <= 1) {
+    select_kernel<kTopK, false><<<plan->cfg.rows, kThreads, plan->smem_select, stream>>>(P);
+    return cudaSuccess;
+  }
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)plan->cfg.rows * (unsigned)k, 1, 1);
+  lc.blockDim = dim3(kThreads, 1, 1);
+  lc.dynamicSmemBytes = plan->smem_select;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)k;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, select_kernel<kTopK, true>, P);
+}
+
+// Configure the cluster kernels for `k` CTAs per row; true when at least one
+// such cluster fits on the device.
+bool cluster_fits(int k, size_t smem) {
+  const void* fns[2] = {(const void*)select_kernel<false, true>, (const void*)select_kernel<true, true>};
+  for (const void* f : fns) {
+    if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+      return false;
+    if (k > 8 && cudaFuncSetAttribute(f, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+      return false;
+    cudaLaunchConfig_t lc = {};
+    lc.gridDim = dim3((unsigned)k, 1, 1);
+    lc.blockDim = dim3(kThreads, 1, 1);
+    lc.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)k;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    lc.attrs = attr;
+    lc.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, f, &lc) != cudaSuccess || clusters < 1) return false;
+  }
+  return true;
 }
 
 }  // namespace
@@ -837,24 +1045,10 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
   const int prm_vec = P.vec_log2g >= 0 ? (kThreads * kVecPerThread) >> P.vec_log2g : 0;
   const int prm_gen = kThreads * kBlocksPerThreadGeneric;
   P.prm = prm_vec > prm_gen ? prm_vec : prm_gen;
-  int cap = P.Kb + 2 * P.prm;
-  if (cap < 2 * P.Kb) cap = 2 * P.Kb;
-  if (cap < 4096) cap = 4096;
-  P.cap = (cap + 255) & ~255;
   P.bitmap_words = (int32_t)((P.nblocks + 31) / 32);
   P.cand_cap = (P.Kb + 1) * P.B + 1;
-  P.scan_prm = kThreads * 8;
-  P.scan_cap = P.K + 2 * P.scan_prm;
-
-  const size_t bitmap_bytes = align16((size_t)P.bitmap_words * 4);
-  const size_t cand_layout = align16((size_t)P.cand_cap * 16 + (size_t)(P.Kb + 1) * 4 +
-                                     (size_t)(P.K > P.cand_cap ? P.K : P.cand_cap) * 4 +
-                                     (size_t)P.K * 4);
-  const size_t stream_bytes = (size_t)P.cap * 8;
-  const size_t region = stream_bytes > cand_layout ? stream_bytes : cand_layout;
-  const size_t smem_select = bitmap_bytes + align16((size_t)P.Kb * 8) + region;
-  const size_t smem_cand = bitmap_bytes + cand_layout;
-  const size_t smem_scan = (size_t)P.scan_cap * 8 + (size_t)P.K * 8;
+  P.scan_prm = kThreads * kVecPerThread;  // groups per streaming round (>= the scalar path's)
+  P.scan_cap = ((P.K + 2 * P.scan_prm) + 255) & ~255;
 
   int dev_count = 0;
   if (cudaGetDeviceCount(&dev_count) != cudaSuccess || device < 0 || device >= dev_count) {
@@ -868,27 +1062,46 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
     return DSA_ERR_CUDA;
   }
   int sms = 0, smem_optin = 0;
-  cudaError_t e1 = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-  cudaError_t e2 = cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
   const size_t static_smem = sizeof(Shared) + 64;
   int rc = DSA_OK;
   int ctas = 0;
-  if (e1 != cudaSuccess || e2 != cudaSuccess) {
+  int split = 1;
+  Sizes z = sizes_for(P, 1);
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
     rc = DSA_ERR_CUDA;
-  } else if (smem_select + static_smem > (size_t)smem_optin || smem_cand + static_smem > (size_t)smem_optin ||
-             smem_scan + static_smem > (size_t)smem_optin) {
-    rc = DSA_ERR_UNSUPPORTED;
-  } else if (cudaFuncSetAttribute(select_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem_select) != cudaSuccess ||
-             cudaFuncSetAttribute(select_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem_select) != cudaSuccess ||
-             cudaFuncSetAttribute(topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem_cand) != cudaSuccess ||
-             cudaFuncSetAttribute(topk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  (int)smem_scan) != cudaSuccess ||
-             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, select_kernel<true>, kThreads,
-                                                           smem_select) != cudaSuccess) {
-    rc = DSA_ERR_CUDA;
+  } else {
+    // CTAs per row: automatic = grow while the whole grid still fits in about
+    // one wave of two CTAs per SM and every CTA keeps >= kMinBlocksPerCta
+    // blocks of a full-width row; or the configured exact value.
+    int want = cfg->split;
+    if (want == 0) {
+      want = 1;
+      while (want < kMaxSplit && (int64_t)cfg->rows * want * 2 <= 2LL * sms &&
+             P.nblocks >= (int64_t)2 * want * kMinBlocksPerCta)
+        want *= 2;
+    }
+    for (split = want; split >= 1; split /= 2) {
+      z = sizes_for(P, split);
+      if (z.select + static_smem > (size_t)smem_optin) continue;
+      if (split == 1 || cluster_fits(split, z.select)) break;
+    }
+    cudaGetLastError();
+    if (split < 1 || z.select + static_smem > (size_t)smem_optin ||
+        z.cand + static_smem > (size_t)smem_optin || z.scan + static_smem > (size_t)smem_optin) {
+      rc = DSA_ERR_UNSUPPORTED;
+    } else if (cudaFuncSetAttribute(select_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)z.select) != cudaSuccess ||
+               cudaFuncSetAttribute(select_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)z.select) != cudaSuccess ||
+               cudaFuncSetAttribute(topk_cand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)z.cand) != cudaSuccess ||
+               cudaFuncSetAttribute(topk_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)z.scan) != cudaSuccess ||
+               cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ctas, select_kernel<true, false>, kThreads,
+                                                             z.select) != cudaSuccess) {
+      rc = DSA_ERR_CUDA;
+    }
   }
   if (prev >= 0 && prev != device) cudaSetDevice(prev);
   if (rc != DSA_OK) {
@@ -900,10 +1113,11 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
   pl->cfg = *cfg;
   pl->device = device;
   pl->sm_count = sms;
+  pl->split = split;
   pl->base = P;
-  pl->smem_select = smem_select;
-  pl->smem_topk_cand = smem_cand;
-  pl->smem_topk_scan = smem_scan;
+  pl->smem_select = z.select;
+  pl->smem_topk_cand = z.cand;
+  pl->smem_topk_scan = z.scan;
   pl->ctas_per_sm_select = ctas;
   *plan = pl;
   if (workspace_bytes) *workspace_bytes = 0;
@@ -926,7 +1140,8 @@ int dsa_plan_describe(const dsa_select_plan* plan, dsa_plan_desc* out) {
   out->smem_topk_cand = (int64_t)plan->smem_topk_cand;
   out->smem_topk_scan = (int64_t)plan->smem_topk_scan;
   out->ctas_per_sm_select = plan->ctas_per_sm_select;
-  out->grid_select = plan->cfg.rows;
+  out->grid_select = plan->cfg.rows * plan->split;
+  out->split = plan->split;
   return DSA_OK;
 }
 
@@ -942,8 +1157,9 @@ static int check_common(const dsa_select_plan* plan, const void* logits, const i
   return DSA_OK;
 }
 
-static int finish_launch() {
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+static int finish_launch(cudaError_t launch) {
+  const cudaError_t last = cudaGetLastError();
+  return (launch == cudaSuccess && last == cudaSuccess) ? DSA_OK : DSA_ERR_CUDA;
 }
 
 int dsa_candidate_select(const dsa_select_plan* plan, float* logits, const int32_t* starts,
@@ -959,8 +1175,7 @@ int dsa_candidate_select(const dsa_select_plan* plan, float* logits, const int32
   P.starts = starts;
   P.ends = ends;
   P.cand = cand;
-  select_kernel<false><<<plan->cfg.rows, kThreads, plan->smem_select, (cudaStream_t)stream>>>(P);
-  return finish_launch();
+  return finish_launch(launch_select<false>(plan, P, (cudaStream_t)stream));
 }
 
 int dsa_select_topk(const dsa_select_plan* plan, float* logits, const int32_t* starts,
@@ -977,8 +1192,7 @@ int dsa_select_topk(const dsa_select_plan* plan, float* logits, const int32_t* s
   P.ends = ends;
   P.cand = cand;
   P.topk = topk;
-  select_kernel<true><<<plan->cfg.rows, kThreads, plan->smem_select, (cudaStream_t)stream>>>(P);
-  return finish_launch();
+  return finish_launch(launch_select<true>(plan, P, (cudaStream_t)stream));
 }
 
 int dsa_row_topk(const dsa_select_plan* plan, const float* logits, const int32_t* starts,
@@ -1000,7 +1214,7 @@ int dsa_row_topk(const dsa_select_plan* plan, const float* logits, const int32_t
   } else {
     topk_scan_kernel<<<plan->cfg.rows, kThreads, plan->smem_topk_scan, (cudaStream_t)stream>>>(P);
   }
-  return finish_launch();
+  return finish_launch(cudaSuccess);
 }
 
 }  // extern "C"

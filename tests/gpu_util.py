@@ -12,7 +12,7 @@ class Case:
     """One call: logits [rows, row_stride] float32 (host) + bounds + shape."""
 
     def __init__(self, logits, starts, ends, *, width, block_size, block_topk, row_topk,
-                 row_repeat=1, causal=True, col_stride=1, row_stride=None):
+                 row_repeat=1, causal=True, col_stride=1, row_stride=None, split=0):
         self.logits = np.ascontiguousarray(logits, dtype=np.float32)
         self.rows = self.logits.shape[0]
         self.starts = None if starts is None else np.asarray(starts, dtype=np.int32)
@@ -25,6 +25,7 @@ class Case:
         self.causal = causal
         self.cs = col_stride
         self.row_stride = self.logits.shape[1] if row_stride is None else row_stride
+        self.split = split
 
     @classmethod
     def from_workload(cls, wl, logits, starts, ends):
@@ -36,7 +37,7 @@ class Case:
         return dict(rows=self.rows, width=self.width, block_size=self.B, block_topk=self.Kb,
                     row_topk=self.K, row_stride=self.row_stride, col_stride=self.cs,
                     row_repeat=self.rep, repeat_causal=self.causal,
-                    has_starts=self.starts is not None)
+                    has_starts=self.starts is not None, split=self.split)
 
     def oracle(self):
         from oracle import default

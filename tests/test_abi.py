@@ -50,7 +50,7 @@ def test_exports_are_c_linkage():
 
 def _init(lib, **kw):
     base = dict(rows=4, width=4096, block_size=8, block_topk=32, row_topk=64)
-    raw = {k: kw.pop(k) for k in ("has_starts", "repeat_causal", "reserved") if k in kw}
+    raw = {k: kw.pop(k) for k in ("has_starts", "repeat_causal", "split") if k in kw}
     base.update(kw)
     cfg = dsa.make_cfg(**base)
     for k, v in raw.items():  # set the raw C fields, bypassing make_cfg's normalisation
@@ -67,13 +67,13 @@ def _init(lib, **kw):
                                 dict(block_size=0), dict(block_topk=0), dict(row_topk=0),
                                 dict(rows=-1), dict(row_repeat=0), dict(col_stride=0),
                                 dict(row_stride=100), dict(has_starts=2), dict(repeat_causal=3),
-                                dict(reserved=1)])
+                                dict(split=3), dict(split=-2)])
 def test_invalid_shapes_rejected_before_cuda(lib, kw):
     assert _init(lib, **kw) == dsa.DSA_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("kw", [dict(row_topk=4097), dict(block_topk=5000),
-                                dict(block_size=5000)])
+                                dict(block_size=5000), dict(split=32)])
 def test_out_of_range_shapes_unsupported(lib, kw):
     assert _init(lib, **kw) == dsa.DSA_ERR_UNSUPPORTED
 

@@ -110,6 +110,52 @@ def test_ascending_values_force_many_compactions():
     check_all_modes(case, what="monotone")
 
 
+@pytest.mark.parametrize("split", [2, 4, 16])
+@pytest.mark.parametrize("layout", ["aligned", "misaligned", "stride2", "b1"])
+def test_cluster_split_rows(split, layout):
+    """k CTAs per row in a thread-block cluster: each streams a share of the
+    blocks, the leader merges the shares over distributed shared memory."""
+    rng = np.random.default_rng(split * 13 + len(layout))
+    W, B, cs, starts = 200_000, 8, 1, [0, 4, 0, 100]
+    if layout == "misaligned":
+        starts = [1, 5, 3, 6]
+    elif layout == "stride2":
+        B, cs = 16, 2
+    elif layout == "b1":
+        W, B = 60_000, 1
+    x = rng.standard_normal((4, W * cs)).astype(np.float32)
+    x[1, ::97] = -np.inf
+    ends = [W, W + 3 * B + 1, 150_001, 3000]
+    case = Case(x, starts, ends, width=W, block_size=B, block_topk=256, row_topk=2048,
+                col_stride=cs, row_stride=W * cs, split=split)
+    run = DeviceRun(case)
+    assert run.plan.describe()["split"] == split
+    check_all_modes(case, what=f"split={split} {layout}")
+
+
+def test_cluster_split_edge_rows():
+    """Cluster path on the hand-worked edge shapes scaled up: start past W,
+    empty rows, pins past W, -NaN blocks, few candidates (-inf tier)."""
+    rng = np.random.default_rng(77)
+    W = 70_001
+    x = rng.standard_normal((8, W)).astype(np.float32)
+    x[3, 10_000:10_800] = np.array([0xFFC00000], dtype=np.uint32).view(np.float32)[0]
+    starts = [W + 5, 0, 0, 0, 17, 0, 3, 0]
+    ends = [W + 20, 0, -4, W, W + 9, 1, 65_000, W + 16]
+    for Kb, K in ((256, 2048), (3, 40), (1, 4096)):
+        case = Case(x, starts, ends, width=W, block_size=8, block_topk=Kb, row_topk=K, split=8)
+        check_all_modes(case, what=f"cluster edges Kb={Kb} K={K}")
+
+
+def test_auto_split_for_few_long_rows():
+    import sparse_attention_indexer_live_gb300 as dsa
+    few = dsa.dsa_select_init(rows=1, width=1 << 20, block_size=8, block_topk=256, row_topk=2048)
+    many = dsa.dsa_select_init(rows=2048, width=1 << 20, block_size=8, block_topk=256,
+                               row_topk=2048)
+    assert few.describe()["split"] >= 8
+    assert many.describe()["split"] == 1
+
+
 def test_tiny_workload_full():
     wl = wk.WORKLOADS["tiny"]
     x, s, e = wk.make_all(wl)
