@@ -79,6 +79,8 @@ struct Params {
   int32_t cand_cap;      // (Kb + 1) * B + 1
   int32_t scan_cap;      // scan-mode streaming buffer entries
   int32_t scan_prm;
+  int32_t epoch;         // streaming rounds between two capacity checks (128-bit path)
+  int32_t scan_epoch;    // the same for the scan-mode buffer
 };
 
 // Scratch with a fixed size, in static shared memory.
@@ -92,6 +94,7 @@ struct Shared {
   uint32_t sel_above;
   uint32_t sel_count;
   int32_t counts[4];
+  int32_t part[kMaxSplit + 1];  // cluster leader: per-CTA counts, then offsets
   uint64_t tau;
 };
 
@@ -213,8 +216,15 @@ __device__ uint64_t select_kth(const uint64_t* a, int n, int k, Shared& sh) {
       }
       const uint32_t act = __ballot_sync(kFull, in);
       if (in) {
-        const uint32_t peers = __match_any_sync(act, d);
-        if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (uint32_t)__popc(peers));
+        // one atomic per warp when its digits agree (the common case in the
+        // leading digits), else one per lane
+        int same = 0;
+        __match_all_sync(act, d, &same);
+        if (!same) {
+          atomicAdd(&sh.hist[d], 1u);
+        } else if (lane == __ffs(act) - 1) {
+          atomicAdd(&sh.hist[d], (uint32_t)__popc(act));
+        }
       }
     }
     __syncthreads();
@@ -276,31 +286,67 @@ __device__ void compact_best(uint64_t* buf, uint64_t* keep, int k, int cap, Shar
 }
 
 // Ids of the set bits of bm among [0, nbits), ascending, into out[0 .. cap);
-// returns the number of set bits.
+// returns the number of set bits.  Each warp owns a contiguous run of words
+// and walks it 32 words at a time; for every non-zero word all 32 lanes write
+// that word's ids in parallel, so the cost does not depend on how the set bits
+// cluster.
 template <typename OutT>
 __device__ int enumerate_bits(const uint32_t* bm, int64_t nbits, OutT* out, int cap, Shared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwords = (int)((nbits + 31) >> 5);
-  const int per = (nwords + kThreads - 1) / kThreads;
-  const int w0 = threadIdx.x * per;
-  const int w1 = min(w0 + per, nwords);
+  const int wpw = (nwords + kWarps - 1) / kWarps;  // words per warp
+  const int w_begin = min(warp * wpw, nwords);
+  const int w_end = min(w_begin + wpw, nwords);
+  const uint32_t tail_mask = (nbits & 31) ? (1u << (uint32_t)(nbits & 31)) - 1u : 0xFFFFFFFFu;
+  auto word = [&](int w) -> uint32_t {
+    if (w >= w_end) return 0u;
+    const uint32_t x = bm[w];
+    return w == nwords - 1 ? (x & tail_mask) : x;
+  };
   int cnt = 0;
-  for (int w = w0; w < w1; ++w) {
-    uint32_t x = bm[w];
-    if ((int64_t)(w + 1) * 32 > nbits) x &= (1u << (uint32_t)(nbits & 31)) - 1u;
-    cnt += __popc(x);
+  for (int c = w_begin; c < w_end; c += 32) cnt += __popc(word(c + lane));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
+  if (lane == 0) sh.warp_tot[warp] = cnt;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < kWarps ? sh.warp_tot[lane] : 0;
+    const int own = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane < kWarps) sh.warp_tot[lane] = v - own;  // exclusive base of each warp
+    if (lane == kWarps - 1) sh.warp_tot[kWarps] = v;  // grand total
   }
-  int total;
-  int pos = block_exclusive_scan(cnt, &total, sh);
-  for (int w = w0; w < w1; ++w) {
-    uint32_t x = bm[w];
-    if ((int64_t)(w + 1) * 32 > nbits) x &= (1u << (uint32_t)(nbits & 31)) - 1u;
-    while (x) {
-      const int b = __ffs(x) - 1;
-      if (pos < cap) out[pos] = (OutT)(w * 32 + b);
-      ++pos;
-      x &= x - 1;
+  __syncthreads();
+  int running = sh.warp_tot[warp];
+  const int total = sh.warp_tot[kWarps];
+  for (int c = w_begin; c < w_end; c += 32) {
+    const uint32_t x = word(c + lane);
+    const int pc = __popc(x);
+    int incl = pc;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int base = running + incl - pc;
+    running += __shfl_sync(kFull, incl, 31);
+    uint32_t nz = __ballot_sync(kFull, x != 0);
+    while (nz) {
+      const int j = __ffs(nz) - 1;
+      nz &= nz - 1;
+      const uint32_t xj = __shfl_sync(kFull, x, j);
+      const int bj = __shfl_sync(kFull, base, j);
+      if ((xj >> lane) & 1u) {
+        const int pos = bj + __popc(xj & lanemask_lt());
+        if (pos < cap) out[pos] = (OutT)((c + j) * 32 + lane);
+      }
     }
   }
+  __syncthreads();  // warp_tot is reused by the next block-wide scan
   return total;
 }
 
@@ -338,10 +384,9 @@ __device__ void stream_block_maxima(const Params& p, const float* rowp, const Ro
     const int32_t v_full = min(v_end, nv_full);
     constexpr int32_t VR = kThreads * kVecPerThread;
     const float filler = __uint_as_float(kFillerBits);
-    for (int32_t rb = j0 << g_log2; rb < v_end; rb += VR) {
-      if (sh.cnt > p.cap - p.prm) compact_best(buf, keep, p.Kb, p.cap, sh);
-      const uint64_t tau = sh.tau;
-      float4 x[kVecPerThread];
+    // one round = kVecPerThread 16-byte vectors per thread; the next round's
+    // loads are in flight while this one is reduced and appended
+    auto load_round = [&](int32_t rb, float4* x) {
 #pragma unroll
       for (int u = 0; u < kVecPerThread; ++u) {
         const int32_t v = rb + (warp * kVecPerThread + u) * 32 + lane;
@@ -358,15 +403,37 @@ __device__ void stream_block_maxima(const Params& p, const float* rowp, const Ro
           }
         }
       }
+    };
+    float4 x[kVecPerThread];
+    int32_t rb = j0 << g_log2;
+    if (rb < v_end) load_round(rb, x);
+    // epochs of p.epoch rounds: the buffer absorbs a whole epoch's worst-case
+    // insertions, so the CTA synchronises (and maybe compacts) once per epoch
+    while (rb < v_end) {
+      // until the first compaction sets a threshold, epochs are one round
+      // long and compaction starts as soon as 2*Kb entries are in
+      const bool first = sh.tau == 0;
+      const int ep = first ? 1 : p.epoch;
+      if (sh.cnt > p.cap - ep * p.prm || (first && sh.cnt >= 2 * p.Kb))
+        compact_best(buf, keep, p.Kb, p.cap, sh);
+      const uint64_t tau = sh.tau;
+      for (int e = 0; e < ep && rb < v_end; ++e) {
+        const int32_t nrb = rb + VR;
+        float4 y[kVecPerThread];
+        if (nrb < v_end) load_round(nrb, y);
 #pragma unroll
-      for (int u = 0; u < kVecPerThread; ++u) {
-        uint32_t m = max4key(x[u]);
-        for (int o = 1; o < g; o <<= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
-        const int32_t v = rb + (warp * kVecPerThread + u) * 32 + lane;
-        const int32_t j = v >> g_log2;
-        const uint64_t c = compose(m, (uint32_t)j);
-        const bool ins = ((lane & (g - 1)) == 0) && j < j1 && c > tau;
-        warp_append(ins, c, buf, &sh.cnt, p.cap);
+        for (int u = 0; u < kVecPerThread; ++u) {
+          uint32_t m = max4key(x[u]);
+          for (int o = 1; o < g; o <<= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
+          const int32_t v = rb + (warp * kVecPerThread + u) * 32 + lane;
+          const int32_t j = v >> g_log2;
+          const uint64_t c = compose(m, (uint32_t)j);
+          const bool ins = ((lane & (g - 1)) == 0) && j < j1 && c > tau;
+          warp_append(ins, c, buf, &sh.cnt, p.cap);
+        }
+#pragma unroll
+        for (int u = 0; u < kVecPerThread; ++u) x[u] = y[u];
+        rb = nrb;
       }
       __syncthreads();
     }
@@ -409,7 +476,8 @@ __device__ void finish_block_topk(const Params& p, const Row& R, int r, uint64_t
   const int take = (int)(p.nblocks < Kb ? p.nblocks : Kb);
   bool lo = false;
   for (int i = threadIdx.x; i < n; i += kThreads) lo |= comp_key(buf[i]) < kKeyNegInf;
-  if (!__syncthreads_or(lo)) {
+  const bool fast = !__syncthreads_or(lo);
+  if (fast) {
     // No kept live block scores below -inf, so the -inf padding blocks rank
     // right after all of them: the set is the live entries plus the first
     // take - n padding ids (n_b, n_b + 1, ...).
@@ -445,7 +513,9 @@ __device__ void finish_block_topk(const Params& p, const Row& R, int r, uint64_t
   }
   __syncthreads();
   int32_t* crow = p.cand + (int64_t)r * (Kb + 1);
-  const int got = min(enumerate_bits(bitmap, p.nblocks, crow, Kb, sh), Kb);
+  // the fast path sets only ids below n_b + (take - n); the general one any
+  const int64_t span = fast ? (int64_t)R.nb + (take - n > 0 ? take - n : 0) : p.nblocks;
+  const int got = min(enumerate_bits(bitmap, span, crow, Kb, sh), Kb);
   for (int i = got + threadIdx.x; i < Kb; i += kThreads) crow[i] = -1;
   __syncthreads();  // every thread is done reading the bitmap before the pin bit goes in
   if (threadIdx.x == 0) {
@@ -603,7 +673,9 @@ __device__ void row_topk_kept(const Params& p, const float* rowp, const Row& R, 
     int pos = block_exclusive_scan(cnt, &total, sh);
     for (int i = i0; i < i1; ++i)
       if (comp[i] != 0 && comp_key(comp[i]) > kKeyNegInf) la[pos++] = (int32_t)comp_index(comp[i]);
-    // scan the masked span for -inf columns, 4 consecutive columns per thread
+    // the first m columns of the span that equal -inf after the mask: every
+    // column that is not kept, and kept columns holding -inf (read: the mask
+    // never changes a kept column), 4 consecutive columns per thread
     int found = 0;
     for (int64_t base = s; base < ec && found < m; base += 4 * kThreads) {
       const int64_t c0 = base + 4 * threadIdx.x;
@@ -611,7 +683,10 @@ __device__ void row_topk_kept(const Params& p, const float* rowp, const Row& R, 
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const int64_t c = c0 + k;
-        if (c < ec && __float_as_uint(__ldcg(rowp + c * cs)) == kNegInfBits) hits |= 1u << k;
+        if (c < ec) {
+          const bool kept = bit_set(bitmap, (c - s) / B) || (edge_extra && c == W - 1);
+          if (!kept || __float_as_uint(__ldcg(rowp + c * cs)) == kNegInfBits) hits |= 1u << k;
+        }
       }
       int tot;
       int q = found + block_exclusive_scan(__popc(hits), &tot, sh);
@@ -723,16 +798,31 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
     if (sh.cnt > p.Kb) compact_best(buf, keep, p.Kb, p.cap, sh);  // local top-Kb
     cl.sync();  // every CTA's list is final
     if (rank == 0) {
-      int n = sh.cnt;
-      for (int q = 1; q < k; ++q) {
-        const Shared* rsh = cl.map_shared_rank(&sh, (unsigned)q);
-        const uint64_t* rbuf = cl.map_shared_rank(buf, (unsigned)q);
-        const int cq = min(rsh->cnt, p.Kb);
-        for (int i = threadIdx.x; i < cq; i += kThreads) buf[n + i] = rbuf[i];
-        n += cq;
+      // every peer's count at once, then all peers' entries in one pass
+      if (threadIdx.x < k) {
+        const int q = threadIdx.x;
+        sh.part[q] = q == 0 ? sh.cnt : min(cl.map_shared_rank(&sh, (unsigned)q)->cnt, p.Kb);
       }
       __syncthreads();
-      if (threadIdx.x == 0) sh.cnt = n;
+      if (threadIdx.x == 0) {
+        int off = 0;
+        for (int q = 0; q < k; ++q) {
+          const int c = sh.part[q];
+          sh.part[q] = off;  // exclusive offset
+          off += c;
+        }
+        sh.part[k] = off;
+      }
+      __syncthreads();
+      const int own = sh.part[1];
+      const int total = sh.part[k];
+      for (int i = own + threadIdx.x; i < total; i += kThreads) {
+        int q = 1;
+        while (q + 1 < k && sh.part[q + 1] <= i) ++q;
+        buf[i] = cl.map_shared_rank(buf, (unsigned)q)[i - sh.part[q]];
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) sh.cnt = total;
       __syncthreads();
       finish_block_topk(p, R, r, buf, keep, bitmap, sh);
     }
@@ -846,6 +936,7 @@ __global__ void __launch_bounds__(kThreads, 2) topk_scan_kernel(const Params p) 
   q.Kb = K;
   q.cap = p.scan_cap;
   q.prm = p.scan_prm;
+  q.epoch = p.scan_epoch;
   Row G = R;
   G.nb = (L + kScanGroup - 1) / kScanGroup;
   stream_block_maxima(q, rowp, G, 0, G.nb, buf, keep, sh);
@@ -937,14 +1028,29 @@ struct Sizes {
 // (the cluster leader's buffer must hold every CTA's top-Kb plus Kb padding).
 Sizes sizes_for(Params& P, int split) {
   int cap = P.Kb + 2 * P.prm;
-  if (cap < 2 * P.Kb) cap = 2 * P.Kb;
+  if (cap < 2 * P.Kb + P.prm) cap = 2 * P.Kb + P.prm;
   if (cap < (split + 1) * P.Kb) cap = (split + 1) * P.Kb;
   if (cap < 4096) cap = 4096;
-  P.cap = (cap + 255) & ~255;
+  cap = (cap + 255) & ~255;
   const size_t bitmap_bytes = align16((size_t)P.bitmap_words * 4);
   const size_t cand_layout = align16((size_t)P.cand_cap * 16 + (size_t)(P.Kb + 1) * 4 +
                                      (size_t)(P.K > P.cand_cap ? P.K : P.cand_cap) * 4 +
                                      (size_t)P.K * 4);
+  // the region holds the larger of the streaming buffer and the row top-k
+  // layout; let the buffer use all of it (longer epochs between barriers)
+  const int cap_region = (int)((cand_layout / 8) & ~(size_t)255);
+  if (cap_region > cap) cap = cap_region;
+  P.cap = cap;
+  // compaction fires once the count exceeds cap - epoch * prm; leave at least
+  // max(Kb, prm) entries of room above the Kb a compaction keeps
+  P.epoch = (cap - P.Kb - (P.Kb > P.prm ? P.Kb : P.prm)) / P.prm;
+  if (P.epoch < 1) P.epoch = 1;
+  if (P.epoch > 8) P.epoch = 8;
+  const int scan_region_entries = P.K * kScanGroup > P.scan_cap ? P.K * kScanGroup : P.scan_cap;
+  P.scan_cap = scan_region_entries & ~255;
+  P.scan_epoch = (P.scan_cap - P.K - (P.K > P.scan_prm ? P.K : P.scan_prm)) / P.scan_prm;
+  if (P.scan_epoch < 1) P.scan_epoch = 1;
+  if (P.scan_epoch > 8) P.scan_epoch = 8;
   const size_t stream_bytes = (size_t)P.cap * 8;
   const size_t region = stream_bytes > cand_layout ? stream_bytes : cand_layout;
   Sizes z;
