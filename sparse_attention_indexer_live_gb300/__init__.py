@@ -9,8 +9,10 @@ from .binding import (DSA_ERR_CUDA, DSA_ERR_INVALID_ARG, DSA_ERR_TIMEOUT, DSA_ER
                       dsa_plan_desc, dsa_row_topk, dsa_select_cfg, dsa_select_init,
                       dsa_select_topk, load, make_cfg, status_string)
 from .build import LIB_PATH, build
+from .sharded import Shard, ShardedSelector, shard_rows
 
 __all__ = ["DSA_OK", "DSA_ERR_INVALID_ARG", "DSA_ERR_UNSUPPORTED", "DSA_ERR_CUDA",
            "DSA_ERR_TIMEOUT", "DsaSelectError", "EXPORTS", "Plan", "dsa_select_cfg",
            "dsa_plan_desc", "make_cfg", "dsa_select_init", "dsa_candidate_select",
-           "dsa_row_topk", "dsa_select_topk", "status_string", "load", "build", "LIB_PATH"]
+           "dsa_row_topk", "dsa_select_topk", "status_string", "load", "build", "LIB_PATH",
+           "Shard", "ShardedSelector", "shard_rows"]
