@@ -384,6 +384,21 @@ def measure_extras(dsa, torch, dev, local, prefill):
         "ms_per_launch": ms, "rows_per_s": wlp.rows / (ms / 1e3),
         "achieved_gbs": scan_alg / (ms / 1e3) / 1e9,
         "matches_fused": bool(torch.equal(out_t, topk_p))}
+    # top-k / sliding-window combine on the prefill chunk's top-k
+    window = 128
+    comb = torch.empty((wlp.rows, wlp.row_topk + window), dtype=torch.int32, device=dev)
+    for _ in range(3):
+        dsa.dsa_combine_window(plan_p, None, ends_p, topk_p, window, comb)
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    for _ in range(20):
+        dsa.dsa_combine_window(plan_p, None, ends_p, topk_p, window, comb)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / 20
+    comb_alg = wlp.rows * (4 * wlp.row_topk + 4 * (wlp.row_topk + window) + 8)
+    out["combine_window_prefill_1m"] = {"window": window, "us_per_launch": us,
+                                        "achieved_gbs": comb_alg / (us * 1e-6) / 1e9}
     return out
 
 

@@ -158,6 +158,19 @@ int dsa_select_topk(const dsa_select_plan* plan, float* logits, const int32_t* s
                     const int32_t* ends, int32_t* cand, int32_t* topk, void* workspace,
                     struct CUstream_st* stream);
 
+/*
+ * Consumer step after the row top-k: per row, the ascending union of its
+ * top-k indices (topk [rows, K] as dsa_row_topk writes them: an ascending
+ * prefix of indices >= 0, then -1) and the last `window` columns of its live
+ * span, [max(start, e' - window), e') with e' = min(end, W), written to
+ * out int32 [rows, K + window] and padded with -1.  vLLM PR #57459 (Speedup
+ * Result) names this step CombineTopkSwaIndicesKernel without defining it;
+ * this is the plain reading.  window >= 0; starts/ends as for the other calls.
+ */
+int dsa_combine_window(const dsa_select_plan* plan, const int32_t* starts, const int32_t* ends,
+                       const int32_t* topk, int32_t window, int32_t* out,
+                       struct CUstream_st* stream);
+
 /* Static description of a status code. */
 const char* dsa_status_string(int status);
 

@@ -62,6 +62,8 @@ def _bind(path: str):
     L.oracle_row_topk.argtypes = [vp, i64, i64, i64, i64, i32, vp]
     L.oracle_row.restype = ctypes.c_int
     L.oracle_row.argtypes = [vp, i64, i64, i64, i64, i32, i32, i32, vp, vp]
+    L.oracle_combine_window.restype = i32
+    L.oracle_combine_window.argtypes = [vp, i32, i64, i64, i64, i32, vp]
     L.oracle_run.restype = ctypes.c_int
     L.oracle_run.argtypes = [vp, i32, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, i32,
                              vp, vp]
@@ -131,6 +133,17 @@ class Oracle:
         out = np.zeros(K, dtype=np.int32)
         n = self.L.oracle_row_topk(row.ctypes.data, width, col_stride, s, e, K,
                                    out.ctypes.data)
+        if n < 0:
+            raise MemoryError
+        return out
+
+    def combine_window(self, topk_row, s, e, width, window):
+        """Union of a row's top-k and the last `window` live columns, ascending,
+        padded with -1 to K + window."""
+        t = np.ascontiguousarray(topk_row, dtype=np.int32)
+        out = np.zeros(len(t) + window, dtype=np.int32)
+        n = self.L.oracle_combine_window(t.ctypes.data, len(t), s, e, width, window,
+                                         out.ctypes.data)
         if n < 0:
             raise MemoryError
         return out

@@ -267,3 +267,30 @@ int oracle_run(float* logits, int32_t rows, int64_t W, int64_t row_stride, int64
   }
   return ORACLE_OK;
 }
+
+/* Consumer step after the row top-k: the top-k and sliding-window index
+ * combine, which vLLM PR #57459 (Speedup Result) names as
+ * CombineTopkSwaIndicesKernel without defining it.  Reading taken: the
+ * ascending union of the row's top-k indices (entries >= 0) and the last
+ * `window` columns of its live span [max(s, e' - window), e'), padded with -1
+ * to K + window entries.  Returns the number of valid entries. */
+int32_t oracle_combine_window(const int32_t* topk, int32_t K, int64_t s, int64_t e, int64_t W,
+                              int32_t window, int32_t* out) {
+  int64_t ec = clamp_end(e, W);
+  int64_t w1 = ec > s ? ec : s;
+  int64_t w0 = w1 - window > s ? w1 - window : s;
+  int64_t cap = (int64_t)K + window;
+  int64_t* all = (int64_t*)malloc((size_t)(cap > 0 ? cap : 1) * sizeof(int64_t));
+  if (!all) return ORACLE_ENOMEM;
+  int64_t n = 0;
+  for (int32_t i = 0; i < K; ++i)
+    if (topk[i] >= 0) all[n++] = topk[i];
+  for (int64_t c = w0; c < w1; ++c) all[n++] = c;
+  qsort(all, (size_t)n, sizeof(int64_t), ascending_i64);
+  int64_t m = 0;
+  for (int64_t i = 0; i < n; ++i)
+    if (m == 0 || all[i] != all[m - 1]) all[m++] = all[i];
+  for (int64_t i = 0; i < cap; ++i) out[i] = i < m ? (int32_t)all[i] : -1;
+  free(all);
+  return (int32_t)m;
+}

@@ -36,7 +36,7 @@ class dsa_plan_desc(ctypes.Structure):
 
 
 EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_candidate_select",
-           "dsa_row_topk", "dsa_select_topk", "dsa_status_string")
+           "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_status_string")
 
 _lib = None
 _lock = threading.Lock()
@@ -72,6 +72,8 @@ def load(path: str | None = None):
             L.dsa_row_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
             L.dsa_select_topk.restype = i32
             L.dsa_select_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
+            L.dsa_combine_window.restype = i32
+            L.dsa_combine_window.argtypes = [vp, vp, vp, vp, ctypes.c_int32, vp, vp]
             L.dsa_status_string.restype = ctypes.c_char_p
             L.dsa_status_string.argtypes = [i32]
             _lib = L
@@ -199,3 +201,20 @@ def dsa_select_topk(plan: Plan, logits, starts, ends, cand, topk, stream=None):
     _check(load().dsa_select_topk(plan.handle, _ptr(logits), _ptr(starts), _ptr(ends),
                                   _ptr(cand), _ptr(topk), None, _stream(stream)),
            "dsa_select_topk")
+
+
+def dsa_combine_window(plan: Plan, starts, ends, topk, window: int, out, stream=None):
+    """Union of each row's top-k and the last `window` live columns into
+    out [rows, K + window] int32 (ascending, -1 padded)."""
+    import torch
+    c = plan.cfg
+    nq = -(-c.rows // c.row_repeat)
+    assert ends.dtype == torch.int32 and ends.is_cuda and ends.numel() >= nq, "ends"
+    assert (starts is None) == (not c.has_starts), "starts"
+    assert topk.dtype == torch.int32 and topk.is_cuda and topk.is_contiguous() and \
+        topk.numel() >= c.rows * c.row_topk, "topk"
+    assert out.dtype == torch.int32 and out.is_cuda and out.is_contiguous() and \
+        out.numel() >= c.rows * (c.row_topk + window), "out: CUDA int32 [rows, K + window]"
+    _check(load().dsa_combine_window(plan.handle, _ptr(starts), _ptr(ends), _ptr(topk),
+                                     int(window), _ptr(out), _stream(stream)),
+           "dsa_combine_window")

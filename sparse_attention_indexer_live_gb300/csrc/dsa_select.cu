@@ -972,6 +972,61 @@ __global__ void __launch_bounds__(kThreads, 2) topk_scan_kernel(const Params p) 
     if (buf[i] != 0 && buf[i] >= X && pos < K) out[pos++] = (int32_t)comp_index(buf[i]);
 }
 
+// Consumer step: the ascending union of each row's top-k indices and the
+// last `window` columns of its live span, padded with -1 to K + window (the
+// top-k / sliding-window combine that vLLM PR #57459 names as
+// CombineTopkSwaIndicesKernel).  The window is one contiguous range, so every
+// output position has a closed form: top-k entries before the window keep
+// their slot, the window follows them, later entries shift by the window minus
+// the entries it absorbed.
+constexpr int kCombineThreads = 256;
+
+__global__ void __launch_bounds__(kCombineThreads) combine_window_kernel(const Params p, const int32_t* topk,
+                                                                         int32_t window, int32_t* out) {
+  __shared__ int s_cnt;
+  const int r = blockIdx.x;
+  const Row R = load_row(p, r);
+  const int K = p.K;
+  const int32_t* t = topk + (int64_t)r * K;
+  const int64_t width = (int64_t)K + window;
+  int32_t* o = out + (int64_t)r * width;
+  const int64_t w1 = R.s + R.L;
+  const int64_t w0 = w1 - window > R.s ? w1 - window : R.s;
+  const int nw = (int)(w1 - w0);
+  if (threadIdx.x == 0) s_cnt = 0;
+  __syncthreads();
+  int mine = 0;
+  for (int i = threadIdx.x; i < K; i += kCombineThreads) mine += t[i] >= 0;
+  atomicAdd(&s_cnt, mine);
+  __syncthreads();
+  const int nt = s_cnt;  // valid entries: an ascending prefix of the list
+  int lo = 0, hi = nt;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (t[mid] < w0) lo = mid + 1; else hi = mid;
+  }
+  const int lb0 = lo;
+  hi = nt;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (t[mid] < w1) lo = mid + 1; else hi = mid;
+  }
+  const int absorbed = lo - lb0;  // top-k entries inside the window
+  for (int i = threadIdx.x; i < nt; i += kCombineThreads) {
+    const int64_t a = t[i];
+    int64_t pos = -1;
+    if (a < w0) pos = i;
+    else if (a >= w1) pos = (int64_t)i - absorbed + nw;
+    if (pos >= 0 && pos < width) o[pos] = (int32_t)a;
+  }
+  for (int j = threadIdx.x; j < nw; j += kCombineThreads) {
+    const int64_t pos = (int64_t)lb0 + j;
+    if (pos < width) o[pos] = (int32_t)(w0 + j);
+  }
+  const int64_t total = (int64_t)nt - absorbed + nw;
+  for (int64_t i = total + threadIdx.x; i < width; i += kCombineThreads) o[i] = -1;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -1320,6 +1375,20 @@ int dsa_row_topk(const dsa_select_plan* plan, const float* logits, const int32_t
   } else {
     topk_scan_kernel<<<plan->cfg.rows, kThreads, plan->smem_topk_scan, (cudaStream_t)stream>>>(P);
   }
+  return finish_launch(cudaSuccess);
+}
+
+int dsa_combine_window(const dsa_select_plan* plan, const int32_t* starts, const int32_t* ends,
+                       const int32_t* topk, int32_t window, int32_t* out, struct CUstream_st* stream) {
+  if (!plan) return DSA_ERR_INVALID_ARG;
+  if (window < 0 || (int64_t)plan->cfg.row_topk + window > INT32_MAX) return DSA_ERR_INVALID_ARG;
+  if (plan->cfg.rows == 0) return DSA_OK;
+  if (!ends || !topk || !out) return DSA_ERR_INVALID_ARG;
+  if (plan->cfg.has_starts ? !starts : starts != nullptr) return DSA_ERR_INVALID_ARG;
+  Params P = plan->base;
+  P.starts = starts;
+  P.ends = ends;
+  combine_window_kernel<<<plan->cfg.rows, kCombineThreads, 0, (cudaStream_t)stream>>>(P, topk, window, out);
   return finish_launch(cudaSuccess);
 }
 

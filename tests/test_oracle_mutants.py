@@ -7,6 +7,7 @@ import os
 import pytest
 
 import oracle
+from tests import test_combine_window as combine
 from tests import test_oracle_pins as pins
 from tests.common import load_golden
 
@@ -34,6 +35,10 @@ MUTANTS = [
     ("edge_wrong_column", "(c == W - 1 && edge)", "(c == W - 2 && edge)"),
     ("packed_column_ignores_start", "if (s + b * (int64_t)B < W)", "if (b * (int64_t)B < W)"),
     ("row_topk_take_one_short", "int64_t take = L < K ? L : K;", "int64_t take = L < K ? L : K - 1;"),
+    ("window_one_short", "int64_t w0 = w1 - window > s ? w1 - window : s;",
+     "int64_t w0 = w1 - window + 1 > s ? w1 - window + 1 : s;"),
+    ("combine_keeps_duplicates", "if (m == 0 || all[i] != all[m - 1]) all[m++] = all[i];",
+     "all[m++] = all[i];"),
 ]
 
 
@@ -42,6 +47,9 @@ def _pins_fail(orc) -> list:
     checks = [("golden:" + c["name"], lambda c=c: pins.test_hand_worked_rows(orc, c))
               for c in load_golden()["cases"]]
     checks += [
+        ("combine_hand", lambda: combine.test_hand_worked(orc)),
+        ("combine_span", lambda: combine.test_full_window_is_the_span(orc)),
+        ("combine_union", lambda: combine.test_set_union_on_random_rows(orc)),
         ("block_scores", lambda: pins.test_hand_worked_block_scores(orc)),
         ("key_order", lambda: pins.test_key_is_total_order(orc)),
         ("brute", lambda: pins.test_brute_force_tiny(orc, False)),
