@@ -171,6 +171,38 @@ int dsa_combine_window(const dsa_select_plan* plan, const int32_t* starts, const
                        const int32_t* topk, int32_t window, int32_t* out,
                        struct CUstream_st* stream);
 
+/*
+ * Indexer logits producer (tensor cores, tcgen05 kind::f8f6f4).
+ *
+ * The pages describe an FP8 "MQA score for every query/KV pair" written to a
+ * [num_q, seq_len] matrix (vLLM PR #48726, Motivation) without the formula.
+ * This build computes, for query t and key s in the query's live span
+ * [start_t, min(end_t, keys)):
+ *     logits[t * out_stride + s] = k_scale[s] * sum_h w[t*heads + h] * max(0, q[t, h, :] . k[s, :])
+ * with q, k in OCP FP8 E4M3 and fp32 accumulation; columns outside the live
+ * span are not written.  Supported: heads == 64, head_dim == 128.
+ *   q        uint8 [queries, 64, 128] (e4m3 bytes), 16-byte aligned
+ *   k        uint8 [keys, 128] (e4m3 bytes), 16-byte aligned
+ *   k_scale  f32 [keys];  w  f32 [queries, 64]
+ *   starts   int32 [queries] or NULL (start 0);  ends  int32 [queries]
+ *   logits   f32 [queries, out_stride] (out_stride >= keys)
+ * Waits inside the kernel are bounded; dsa_indexer_status() (synchronising)
+ * reports DSA_ERR_TIMEOUT once if one gave up, and clears it.
+ */
+typedef struct dsa_indexer_cfg {
+  int32_t queries;
+  int32_t keys;
+  int32_t heads;
+  int32_t head_dim;
+  int64_t out_stride;
+} dsa_indexer_cfg;
+
+int dsa_indexer_logits(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k,
+                       const float* k_scale, const float* w, const int32_t* starts,
+                       const int32_t* ends, float* logits, struct CUstream_st* stream);
+
+int dsa_indexer_status(void);
+
 /* Static description of a status code. */
 const char* dsa_status_string(int status);
 

@@ -64,6 +64,10 @@ def _bind(path: str):
     L.oracle_row.argtypes = [vp, i64, i64, i64, i64, i32, i32, i32, vp, vp]
     L.oracle_combine_window.restype = i32
     L.oracle_combine_window.argtypes = [vp, i32, i64, i64, i64, i32, vp]
+    L.oracle_e4m3.restype = ctypes.c_double
+    L.oracle_e4m3.argtypes = [ctypes.c_uint8]
+    L.oracle_indexer_logits.restype = ctypes.c_int
+    L.oracle_indexer_logits.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i64]
     L.oracle_run.restype = ctypes.c_int
     L.oracle_run.argtypes = [vp, i32, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, i32,
                              vp, vp]
@@ -146,6 +150,29 @@ class Oracle:
                                          out.ctypes.data)
         if n < 0:
             raise MemoryError
+        return out
+
+    def e4m3(self, b: int) -> float:
+        return float(self.L.oracle_e4m3(int(b)))
+
+    def indexer_logits(self, q, k, k_scale, w, starts, ends, out):
+        """q [T, H, D] uint8 (e4m3), k [S, D] uint8, k_scale [S] f32, w [T, H]
+        f32, bounds [T]; writes out [T, ld] f32 over each live span."""
+        q = np.ascontiguousarray(q, dtype=np.uint8)
+        k = np.ascontiguousarray(k, dtype=np.uint8)
+        ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+        w = np.ascontiguousarray(w, dtype=np.float32)
+        T, H, D = q.shape
+        S = k.shape[0]
+        st = None if starts is None else np.ascontiguousarray(starts, dtype=np.int32)
+        en = np.ascontiguousarray(ends, dtype=np.int32)
+        assert out.dtype == np.float32 and out.flags.c_contiguous
+        rc = self.L.oracle_indexer_logits(q.ctypes.data, k.ctypes.data, ks.ctypes.data,
+                                          w.ctypes.data, T, S, H, D,
+                                          None if st is None else st.ctypes.data,
+                                          en.ctypes.data, out.ctypes.data, out.shape[1])
+        if rc != OK:
+            raise RuntimeError(f"oracle_indexer_logits: {rc}")
         return out
 
     # ---- whole path -----------------------------------------------------

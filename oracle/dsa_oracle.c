@@ -294,3 +294,70 @@ int32_t oracle_combine_window(const int32_t* topk, int32_t K, int64_t s, int64_t
   free(all);
   return (int32_t)m;
 }
+
+/* ------------------------------------------------------------------------
+ * Indexer logits (the producer in front of the selection path).  The vLLM
+ * pages describe an FP8 "MQA score for every query/KV pair" written to a
+ * [num_q, seq_len] matrix (vLLM PR #48726, Motivation) but print no formula.
+ * Reading taken: H query heads share one key (multi-query), each head's score
+ * is the dot product of e4m3 vectors, and
+ *     logit[t][s] = k_scale[s] * sum_h w[t][h] * max(0, q[t][h] . k[s]),
+ * written only for s in the query's live span [start, min(end, S)).
+ * Plain fp64 arithmetic, rounded once to fp32. */
+
+/* OCP FP8 E4M3: 1 sign, 4 exponent (bias 7), 3 mantissa bits; exponent 0
+ * is subnormal (m * 2^-9); S.1111.111 is NaN; there are no infinities. */
+double oracle_e4m3(uint8_t b) {
+  int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) {
+    uint64_t nan_bits = 0x7FF8000000000000ull;
+    memcpy(&v, &nan_bits, sizeof(v));
+    return v;
+  }
+  if (e == 0) {
+    v = (double)m / 512.0; /* m * 2^-3 * 2^-6 */
+  } else {
+    v = (1.0 + (double)m / 8.0);
+    int x = e - 7;
+    while (x > 0) { v *= 2.0; --x; }
+    while (x < 0) { v /= 2.0; ++x; }
+  }
+  return sign ? -v : v;
+}
+
+int oracle_indexer_logits(const uint8_t* q, const uint8_t* k, const float* k_scale, const float* w,
+                          int32_t T, int32_t S, int32_t H, int32_t D, const int32_t* starts,
+                          const int32_t* ends, float* out, int64_t ld) {
+  if (T < 0 || S < 0 || H < 1 || D < 1 || !q || !k || !k_scale || !w || !ends || !out)
+    return ORACLE_EINVAL;
+  /* decode every byte once */
+  double table[256];
+  for (int i = 0; i < 256; ++i) table[i] = oracle_e4m3((uint8_t)i);
+  double* kd = (double*)malloc((size_t)(S > 0 ? S : 1) * D * sizeof(double));
+  double* qd = (double*)malloc((size_t)H * D * sizeof(double));
+  if (!kd || !qd) {
+    free(kd);
+    free(qd);
+    return ORACLE_ENOMEM;
+  }
+  for (int64_t i = 0; i < (int64_t)S * D; ++i) kd[i] = table[k[i]];
+  for (int32_t t = 0; t < T; ++t) {
+    for (int64_t i = 0; i < (int64_t)H * D; ++i) qd[i] = table[q[(int64_t)t * H * D + i]];
+    int64_t s0 = starts ? starts[t] : 0;
+    int64_t s1 = ends[t] < S ? ends[t] : S;
+    if (s0 < 0) s0 = 0;
+    for (int64_t s = s0; s < s1; ++s) {
+      double acc = 0.0;
+      for (int32_t h = 0; h < H; ++h) {
+        double dot = 0.0;
+        for (int32_t d = 0; d < D; ++d) dot += qd[(int64_t)h * D + d] * kd[s * D + d];
+        if (dot > 0) acc += (double)w[(int64_t)t * H + h] * dot;
+      }
+      out[(int64_t)t * ld + s] = (float)(acc * (double)k_scale[s]);
+    }
+  }
+  free(kd);
+  free(qd);
+  return ORACLE_OK;
+}

@@ -36,7 +36,13 @@ class dsa_plan_desc(ctypes.Structure):
 
 
 EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_candidate_select",
-           "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_status_string")
+           "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_indexer_logits",
+           "dsa_indexer_status", "dsa_status_string")
+
+
+class dsa_indexer_cfg(ctypes.Structure):
+    _fields_ = [("queries", ctypes.c_int32), ("keys", ctypes.c_int32), ("heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("out_stride", ctypes.c_int64)]
 
 _lib = None
 _lock = threading.Lock()
@@ -74,6 +80,11 @@ def load(path: str | None = None):
             L.dsa_select_topk.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp]
             L.dsa_combine_window.restype = i32
             L.dsa_combine_window.argtypes = [vp, vp, vp, vp, ctypes.c_int32, vp, vp]
+            L.dsa_indexer_logits.restype = i32
+            L.dsa_indexer_logits.argtypes = [ctypes.POINTER(dsa_indexer_cfg), vp, vp, vp, vp, vp,
+                                             vp, vp, vp]
+            L.dsa_indexer_status.restype = i32
+            L.dsa_indexer_status.argtypes = []
             L.dsa_status_string.restype = ctypes.c_char_p
             L.dsa_status_string.argtypes = [i32]
             _lib = L
@@ -218,3 +229,28 @@ def dsa_combine_window(plan: Plan, starts, ends, topk, window: int, out, stream=
     _check(load().dsa_combine_window(plan.handle, _ptr(starts), _ptr(ends), _ptr(topk),
                                      int(window), _ptr(out), _stream(stream)),
            "dsa_combine_window")
+
+
+def dsa_indexer_logits(q, k, k_scale, w, starts, ends, logits, stream=None):
+    """Indexer logits on the tensor cores: q [T, 64, 128] and k [S, 128] as
+    uint8 e4m3 bytes, k_scale [S] f32, w [T, 64] f32, bounds [T] int32,
+    logits [T, ld] f32 written over each query's live span."""
+    import torch
+    T, H, D = q.shape
+    S = k.shape[0]
+    for name, t, dt in (("q", q, torch.uint8), ("k", k, torch.uint8), ("k_scale", k_scale,
+                        torch.float32), ("w", w, torch.float32), ("ends", ends, torch.int32)):
+        assert t.dtype == dt and t.is_cuda and t.is_contiguous(), name
+    assert starts is None or (starts.dtype == torch.int32 and starts.is_cuda)
+    assert logits.dtype == torch.float32 and logits.is_cuda and logits.dim() == 2 and \
+        logits.stride(1) == 1 and logits.shape[0] == T and logits.shape[1] >= S
+    cfg = dsa_indexer_cfg(queries=T, keys=S, heads=H, head_dim=D, out_stride=logits.stride(0))
+    _check(load().dsa_indexer_logits(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w),
+                                     _ptr(starts), _ptr(ends), _ptr(logits), _stream(stream)),
+           "dsa_indexer_logits")
+
+
+def dsa_indexer_status() -> int:
+    """DSA_OK, or DSA_ERR_TIMEOUT once after an indexer kernel gave up a wait
+    (synchronises the device)."""
+    return int(load().dsa_indexer_status())

@@ -257,3 +257,40 @@ def make_all(wl: Workload, out: np.ndarray | None = None):
         out = np.empty((wl.rows, wl.row_stride), dtype=np.float32)
     fill_rows(wl, range(wl.rows), out, starts, ends)
     return out, starts, ends
+
+
+# ---------------------------------------------------------------------------
+# indexer producer inputs: e4m3 bytes for q [T, 64, 128] and k [S, 128]
+
+_S_Q = 111
+_S_K = 112
+_S_W = 113
+_S_KS = 114
+
+
+def e4m3_bytes(seed: int, stream: int, row: int, n: int) -> np.ndarray:
+    """n random OCP E4M3 bytes with exponent field in [3, 9] (|value| in
+    [2^-4, 7.5]); no NaN, no subnormal."""
+    x = u32(seed, stream, row, n)
+    sign = (x >> 31) & 1
+    exp = 3 + (x % 7)
+    man = (x >> 8) & 7
+    return ((sign << 7) | (exp << 3) | man).astype(np.uint8)
+
+
+def indexer_inputs(T: int, S: int, seed: int = 7, heads: int = 64, dim: int = 128,
+                   causal: bool = True):
+    """(q, k, k_scale, w, starts, ends) for T queries over S keys; causal ends
+    S - T + t + 1 (the last query sees every key), starts 0."""
+    q = e4m3_bytes(seed, _S_Q, 0, T * heads * dim).reshape(T, heads, dim)
+    k = e4m3_bytes(seed, _S_K, 0, S * dim).reshape(S, dim)
+    ks = (0.5 + _unit(u32(seed, _S_KS, 0, S))).astype(np.float32)
+    a = u32(seed, _S_W, 0, 2 * T * heads)
+    u1, u2 = _unit(a[0::2]), _unit(a[1::2])
+    w = (0.1 * np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)).astype(np.float32)
+    w = w.reshape(T, heads)
+    if causal:
+        ends = (S - T + 1 + np.arange(T)).clip(0, S).astype(np.int32)
+    else:
+        ends = np.full(T, S, dtype=np.int32)
+    return q, k, ks, w, None, ends
