@@ -399,7 +399,42 @@ def measure_extras(dsa, torch, dev, local, prefill):
     comb_alg = wlp.rows * (4 * wlp.row_topk + 4 * (wlp.row_topk + window) + 8)
     out["combine_window_prefill_1m"] = {"window": window, "us_per_launch": us,
                                         "achieved_gbs": comb_alg / (us * 1e-6) / 1e9}
+    out["indexer_producer"] = measure_producer(dsa, torch, dev)
     return out
+
+
+def fp8_peak_tflops():
+    """Measured bf16 burst (MEASURED_PEAKS.json) x the nominal fp8 / bf16
+    dense ratio of 2 (4.5 / 2.25 PFLOP/s); fallback 1.9 PFLOP/s bf16."""
+    try:
+        with open(PEAKS) as f:
+            return 2.0 * float(json.load(f)["bf16_tflops"]), "2 x measured bf16 burst"
+    except Exception:
+        return 2.0 * 1900.0, "2 x fallback bf16 (1.9 PFLOP/s)"
+
+
+def measure_producer(dsa, torch, dev, T=608, S=131072):
+    """FP8 indexer logits on the tensor cores (causal spans)."""
+    q, k, ks, w, _, ends = wk.indexer_inputs(T, S, seed=11)
+    qd, kd = torch.from_numpy(q).to(dev), torch.from_numpy(k).to(dev)
+    ksd, wd = torch.from_numpy(ks).to(dev), torch.from_numpy(w).to(dev)
+    en = torch.from_numpy(ends).to(dev)
+    out = torch.empty((T, S), dtype=torch.float32, device=dev)
+    for _ in range(3):
+        dsa.dsa_indexer_logits(qd, kd, ksd, wd, None, en, out)
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    for _ in range(10):
+        dsa.dsa_indexer_logits(qd, kd, ksd, wd, None, en, out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / 10
+    pairs = int(np.minimum(ends, S).astype(np.int64).sum())
+    flops = 2.0 * pairs * 64 * 128
+    peak, src = fp8_peak_tflops()
+    tf = flops / (ms / 1e3) / 1e12
+    return {"queries": T, "keys": S, "ms_per_launch": ms, "tflops": tf, "peak_tflops": peak,
+            "frac": tf / peak, "peak_source": src, "status": dsa.dsa_indexer_status()}
 
 
 # ---------------------------------------------------------------------------
@@ -541,6 +576,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_1m", choices=sorted(wk.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--producer-only", nargs=2, type=int, metavar=("QUERIES", "KEYS"),
+                    help="time only the tensor-core indexer-logits producer and print its JSON")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the supplementary decode / single-row / scan-mode timings")
     ap.add_argument("--rows", type=int, default=None,
@@ -550,6 +587,16 @@ def main():
     args = ap.parse_args()
     if args.warmup < 1:
         ap.error("--warmup must be >= 1")
+    if args.producer_only:
+        import torch
+
+        import sparse_attention_indexer_live_gb300 as dsa
+        dsa.build()
+        dsa.load()
+        T, S = args.producer_only
+        print(json.dumps(measure_producer(dsa, torch, torch.device("cuda:0"), T=T, S=S)),
+              flush=True)
+        return
     wl = wk.WORKLOADS[args.workload]
     if args.rows is not None:
         wl = wl.with_(rows=args.rows)

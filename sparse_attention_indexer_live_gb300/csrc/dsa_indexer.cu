@@ -17,8 +17,9 @@
 //               of 128B-swizzled shared memory (cp.async.bulk.tensor + mbarrier)
 //   warp 1      tcgen05.mma issuer (kind::f8f6f4, fp32 accumulator in TMEM,
 //               two 256-column accumulators so MMA and epilogue overlap)
-//   warps 2-5   epilogue: tcgen05.ld of a key row, weighted ReLU sum per query,
-//               coalesced fp32 stores of the live span
+//   warps 2-17  epilogue: four warps per TMEM lane quarter, each reading its key
+//               row's 64 columns of one query with tcgen05.ld, weighted ReLU sum
+//               over the heads, coalesced fp32 stores of the live span
 // Every mbarrier wait is bounded by a clock limit; a wait that runs out sets a
 // device error word (read by dsa_indexer_status) and the CTA winds down.
 
@@ -41,7 +42,8 @@ constexpr int kKStep = 32;                     // e4m3 K per tcgen05.mma
 constexpr int kStages = 4;
 constexpr int kTileK = kM * kDim;              // 16 KB
 constexpr int kTileQ = kN * kDim;              // 32 KB
-constexpr int kThreads = 192;                  // 6 warps
+constexpr int kEpiWarps = 16;                  // a multiple of 4: warps per TMEM lane quarter x 4
+constexpr int kThreads = (2 + kEpiWarps) * 32; // TMA warp, MMA warp, epilogue warps
 constexpr uint32_t kTmemCols = 512;            // two fp32 accumulators of 256 columns
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
 
@@ -138,18 +140,6 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // Dynamic shared memory, from a 1024-aligned base:
 //   Q tile [256 x 128 B] | K ring [4 x 128 x 128 B] | mbarriers | TMEM address | w [4 x 64] f32
 constexpr int kOffK = kTileQ;
@@ -200,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&accf[i], 1);
-      mbar_init(&acce[i], 4 * 32);
+      mbar_init(&acce[i], kEpiWarps * 32);
     }
     mbar_init(qbar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -254,37 +244,86 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else if (warp >= 2) {
-      // epilogue: thread = key row m of the tile (TMEM lane), warp % 4 picks the lane quarter
+      // epilogue: thread = key row m of the tile (TMEM lane); warp % 4 picks the
+      // lane quarter, the warps of a quarter split the four queries
+      constexpr int kQueriesPerWarp = kQueriesPerCta * 4 / kEpiWarps;
       const int sub = warp & 3;
+      const int q0 = ((warp - 2) >> 2) * kQueriesPerWarp;
       const int m = sub * 32 + lane;
       const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
-      for (int i = 0; i < ntiles; ++i) {
+      const float4* w4 = reinterpret_cast<const float4*>(ws);
+      // this warp's queries' live spans, read once
+      int64_t qs0[kQueriesPerWarp], qs1[kQueriesPerWarp];
+#pragma unroll
+      for (int j = 0; j < kQueriesPerWarp; ++j) {
+        const int q = q0 + j;
+        qs0[j] = 0;
+        qs1[j] = 0;
+        if (q < nq) {
+          const int t = t0 + q;
+          const int64_t a0 = p.starts ? (int64_t)p.starts[t] : 0;
+          qs0[j] = a0 > 0 ? a0 : 0;
+          qs1[j] = min((int64_t)p.ends[t], (int64_t)p.S);
+        }
+      }
+      int64_t s = klo + m;
+      float ksc = s < khi ? p.k_scale[s] : 0.f;
+      for (int i = 0; i < ntiles; ++i, s += kM) {
         const int a = i & 1;
+        // the next tile's key scale is read while this tile is reduced
+        const int64_t sn = s + kM;
+        const float ksc_next = sn < khi ? p.k_scale[sn] : 0.f;
         if (!mbar_wait(&accf[a], (i >> 1) & 1)) break;
         tc_fence_after();
-        const int64_t s = klo + (int64_t)i * kM + m;
-        const float ksc = s < khi ? p.k_scale[s] : 0.f;
 #pragma unroll 1
-        for (int q = 0; q < kQueriesPerCta; ++q) {
-          float acc = 0.f;
+        for (int q = q0; q < q0 + kQueriesPerWarp; ++q) {
+          uint32_t r0[32], r1[32];
+          const uint32_t col = lane_addr + (uint32_t)(a * kN + q * kHeads);
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+              "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+              : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]),
+                "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]),
+                "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]), "=r"(r0[18]), "=r"(r0[19]),
+                "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]), "=r"(r0[24]), "=r"(r0[25]),
+                "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]), "=r"(r0[30]), "=r"(r0[31])
+              : "r"(col));
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+              "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+              : "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]),
+                "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]),
+                "=r"(r1[14]), "=r"(r1[15]), "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]),
+                "=r"(r1[20]), "=r"(r1[21]), "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]),
+                "=r"(r1[26]), "=r"(r1[27]), "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31])
+              : "r"(col + 32u));
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          // four independent partial sums (one per float4 lane) keep the FMA
+          // dependency chains short
+          float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t r[32];
-            tmem_ld32(lane_addr + (uint32_t)(a * kN + q * kHeads + half * 32), r);
+          for (int j = 0; j < 8; ++j) {
+            const float4 wv = w4[q * (kHeads / 4) + j];
+            acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r0[4 * j + 0]), 0.f), acc0);
+            acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r0[4 * j + 1]), 0.f), acc1);
+            acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r0[4 * j + 2]), 0.f), acc2);
+            acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r0[4 * j + 3]), 0.f), acc3);
+          }
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              acc = fmaf(ws[q * kHeads + half * 32 + j], fmaxf(__uint_as_float(r[j]), 0.f), acc);
+          for (int j = 0; j < 8; ++j) {
+            const float4 wv = w4[q * (kHeads / 4) + 8 + j];
+            acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r1[4 * j + 0]), 0.f), acc0);
+            acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r1[4 * j + 1]), 0.f), acc1);
+            acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r1[4 * j + 2]), 0.f), acc2);
+            acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r1[4 * j + 3]), 0.f), acc3);
           }
-          if (q < nq) {
-            const int t = t0 + q;
-            int64_t s0 = p.starts ? (int64_t)p.starts[t] : 0;
-            if (s0 < 0) s0 = 0;
-            const int64_t s1 = min((int64_t)p.ends[t], (int64_t)p.S);
-            if (s >= s0 && s < s1) p.out[(int64_t)t * p.ld + s] = acc * ksc;
-          }
+          const float acc = (acc0 + acc1) + (acc2 + acc3);
+          const int j = q - q0;
+          if (s >= qs0[j] && s < qs1[j]) p.out[(int64_t)(t0 + q) * p.ld + s] = acc * ksc;
         }
         tc_fence_before();
         mbar_arrive(&acce[a]);
+        ksc = ksc_next;
       }
     }
   }
