@@ -45,7 +45,21 @@ constexpr int kTileQ = kN * kDim;              // 32 KB
 constexpr int kEpiWarps = 16;                  // a multiple of 4: warps per TMEM lane quarter x 4
 constexpr int kThreads = (2 + kEpiWarps) * 32; // TMA warp, MMA warp, epilogue warps
 constexpr uint32_t kTmemCols = 512;            // two fp32 accumulators of 256 columns
+// Bounded waits.  A separate test build (tests/test_gpu_indexer_timeout.py)
+// defines DSA_INDEXER_TEST_WAIT_CYCLES to shorten the limit and
+// DSA_INDEXER_TEST_STARVE to make the first K stage expect one chunk more than
+// its copy delivers, so that wait runs out without any fault; the product
+// build defines neither.
+#ifdef DSA_INDEXER_TEST_WAIT_CYCLES
+constexpr long long kWaitCycles = DSA_INDEXER_TEST_WAIT_CYCLES;
+#else
 constexpr long long kWaitCycles = 4000000000ll;  // ~2 s at 2 GHz
+#endif
+#ifdef DSA_INDEXER_TEST_STARVE
+constexpr uint32_t kStarveBytes = 16;
+#else
+constexpr uint32_t kStarveBytes = 0;
+#endif
 
 // f32 accumulator, A = B = E4M3, both K-major, N = 256, M = 128.
 constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kN >> 3) << 17) |
@@ -219,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < ntiles; ++i) {
         const int st = i % kStages;
         if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) break;
-        mbar_expect_tx(&full[st], kTileK);
+        mbar_expect_tx(&full[st], kTileK + (i == 0 ? kStarveBytes : 0u));
         tma_load_2d(&tk, &full[st], sk + st * kTileK, 0, (int)(klo + (int64_t)i * kM));
       }
     } else if (warp == 1 && lane == 0) {
