@@ -203,6 +203,40 @@ int dsa_indexer_logits(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8
 
 int dsa_indexer_status(void);
 
+/*
+ * The producer fused with the selection, the [queries, keys] logits never
+ * written.  Each query's logits are the ones dsa_indexer_logits computes
+ * (start 0, live span [0, min(end_t, keys))); the launch reduces them to block
+ * maxima and a streaming top-Kb per query while they are still in registers,
+ * keeping every kept block's B values beside it, and leaves one record per
+ * query in `workspace`.  A second launch finishes the block top-k (pin,
+ * packed-column clamp, edge flag) and takes the row top-k exactly as
+ * dsa_select_topk does on the materialised logits: cand and topk are
+ * bit-identical to dsa_indexer_logits followed by dsa_select_topk.  No masked
+ * logits are produced (there is no logits matrix).  The pages materialise the
+ * score matrix (vLLM PR #48726, Motivation; vLLM PR #57459, Summary); the
+ * fusion is this library's own.
+ *   plan       from dsa_select_init with rows == queries, width == keys,
+ *              col_stride 1, has_starts 0, row_repeat 1, block_size in
+ *              {1, 2, 4, 8} and block_topk <= 256; any other plan gives
+ *              DSA_ERR_UNSUPPORTED
+ *   cfg        queries == plan rows, keys == plan width, heads 64, head_dim 128
+ *   q, k, k_scale, w, ends   as for dsa_indexer_logits (no starts)
+ *   workspace  device memory, 16-byte aligned, of at least
+ *              dsa_indexer_select_workspace() bytes; owned by the caller and
+ *              overwritten by every call, so calls that may overlap in time
+ *              need workspaces of their own
+ *   cand, topk int32 [queries, Kb + 1] and [queries, K], as dsa_select_topk
+ * Returns DSA_OK once both launches are queued; bounded-wait timeouts are
+ * reported by dsa_indexer_status() as for dsa_indexer_logits.
+ */
+int dsa_indexer_select_workspace(const dsa_select_plan* plan, size_t* bytes);
+
+int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, const uint8_t* q,
+                       const uint8_t* k, const float* k_scale, const float* w, const int32_t* ends,
+                       void* workspace, size_t workspace_bytes, int32_t* cand, int32_t* topk,
+                       struct CUstream_st* stream);
+
 /* Static description of a status code. */
 const char* dsa_status_string(int status);
 

@@ -7,7 +7,7 @@ Python binding over it.
 from .binding import (DSA_ERR_CUDA, DSA_ERR_INVALID_ARG, DSA_ERR_TIMEOUT, DSA_ERR_UNSUPPORTED,
                       DSA_OK, DsaSelectError, EXPORTS, Plan, dsa_candidate_select,
                       dsa_combine_window, dsa_indexer_cfg, dsa_indexer_logits,
-                      dsa_indexer_status,
+                      dsa_indexer_select, dsa_indexer_select_workspace, dsa_indexer_status,
                       dsa_plan_desc, dsa_row_topk, dsa_select_cfg, dsa_select_init,
                       dsa_select_topk, load, make_cfg, status_string)
 from .build import LIB_PATH, build
@@ -17,5 +17,6 @@ __all__ = ["DSA_OK", "DSA_ERR_INVALID_ARG", "DSA_ERR_UNSUPPORTED", "DSA_ERR_CUDA
            "DSA_ERR_TIMEOUT", "DsaSelectError", "EXPORTS", "Plan", "dsa_select_cfg",
            "dsa_plan_desc", "make_cfg", "dsa_select_init", "dsa_candidate_select",
            "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_indexer_cfg",
-           "dsa_indexer_logits", "dsa_indexer_status", "status_string", "load", "build", "LIB_PATH",
+           "dsa_indexer_logits", "dsa_indexer_select", "dsa_indexer_select_workspace",
+           "dsa_indexer_status", "status_string", "load", "build", "LIB_PATH",
            "Shard", "ShardedSelector", "shard_rows"]

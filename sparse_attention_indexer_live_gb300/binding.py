@@ -37,7 +37,8 @@ class dsa_plan_desc(ctypes.Structure):
 
 EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_candidate_select",
            "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_indexer_logits",
-           "dsa_indexer_status", "dsa_status_string")
+           "dsa_indexer_status", "dsa_indexer_select_workspace", "dsa_indexer_select",
+           "dsa_status_string")
 
 
 class dsa_indexer_cfg(ctypes.Structure):
@@ -85,6 +86,11 @@ def load(path: str | None = None):
                                              vp, vp, vp]
             L.dsa_indexer_status.restype = i32
             L.dsa_indexer_status.argtypes = []
+            L.dsa_indexer_select_workspace.restype = i32
+            L.dsa_indexer_select_workspace.argtypes = [vp, ctypes.POINTER(ctypes.c_size_t)]
+            L.dsa_indexer_select.restype = i32
+            L.dsa_indexer_select.argtypes = [vp, ctypes.POINTER(dsa_indexer_cfg), vp, vp, vp, vp,
+                                             vp, vp, ctypes.c_size_t, vp, vp, vp]
             L.dsa_status_string.restype = ctypes.c_char_p
             L.dsa_status_string.argtypes = [i32]
             _lib = L
@@ -248,6 +254,37 @@ def dsa_indexer_logits(q, k, k_scale, w, starts, ends, logits, stream=None):
     _check(load().dsa_indexer_logits(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w),
                                      _ptr(starts), _ptr(ends), _ptr(logits), _stream(stream)),
            "dsa_indexer_logits")
+
+
+def dsa_indexer_select_workspace(plan: Plan) -> int:
+    """Workspace bytes dsa_indexer_select needs for this plan."""
+    n = ctypes.c_size_t(0)
+    _check(load().dsa_indexer_select_workspace(plan.handle, ctypes.byref(n)),
+           "dsa_indexer_select_workspace")
+    return int(n.value)
+
+
+def dsa_indexer_select(plan: Plan, q, k, k_scale, w, ends, workspace, cand, topk, stream=None):
+    """The indexer logits fused with the selection (never materialised):
+    q [T, 64, 128] and k [S, 128] uint8 e4m3 bytes, k_scale [S] f32, w [T, 64]
+    f32, ends [T] int32; workspace a CUDA uint8 tensor of at least
+    dsa_indexer_select_workspace(plan) bytes; cand [T, Kb + 1], topk [T, K]."""
+    import torch
+    T, H, D = q.shape
+    S = k.shape[0]
+    for name, t, dt in (("q", q, torch.uint8), ("k", k, torch.uint8), ("k_scale", k_scale,
+                        torch.float32), ("w", w, torch.float32), ("ends", ends, torch.int32),
+                        ("workspace", workspace, torch.uint8)):
+        assert t.dtype == dt and t.is_cuda and t.is_contiguous(), name
+    c = plan.cfg
+    for name, t, cols in (("cand", cand, c.block_topk + 1), ("topk", topk, c.row_topk)):
+        assert t.dtype == torch.int32 and t.is_cuda and t.is_contiguous() and \
+            t.numel() >= c.rows * cols, f"{name}: CUDA int32 [rows, {cols}]"
+    cfg = dsa_indexer_cfg(queries=T, keys=S, heads=H, head_dim=D, out_stride=S)
+    _check(load().dsa_indexer_select(plan.handle, ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(k_scale),
+                                     _ptr(w), _ptr(ends), _ptr(workspace), workspace.numel(),
+                                     _ptr(cand), _ptr(topk), _stream(stream)),
+           "dsa_indexer_select")
 
 
 def dsa_indexer_status() -> int:

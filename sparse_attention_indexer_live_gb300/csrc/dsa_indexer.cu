@@ -3,8 +3,7 @@
 //
 // The vLLM pages describe an FP8 "MQA score for every query/KV pair" written
 // to a [num_q, seq_len] matrix (vLLM PR #48726, Motivation) without printing
-// the formula.  Reading taken (the same in the CPU oracle): H query heads
-// share one key, and
+// the formula.  Reading taken: H query heads share one key, and
 //     logit[t][s] = k_scale[s] * sum_h w[t][h] * max(0, q[t][h] . k[s])
 // with e4m3 q, k; written only over the query's live span [start, min(end, S)),
 // the rest of the row is left as it was.
@@ -20,6 +19,15 @@
 //   warps 2-17  epilogue: four warps per TMEM lane quarter, each reading its key
 //               row's 64 columns of one query with tcgen05.ld, weighted ReLU sum
 //               over the heads, coalesced fp32 stores of the live span
+// Fused form (dsa_indexer_select): the same epilogue values, never stored.
+// Each query's four warps reduce them to block maxima (shuffles across B
+// lanes) and keep a streaming top-Kb of blocks in shared memory: a slot per
+// block that beats the running threshold, its B values beside it, plus a copy
+// of the last live block's values.  One reducing barrier per tile decides, for
+// the four warps together, whether the 512-slot buffer must be compacted
+// (bitonic sort of a copy, keep the Kb best, rebuild the free-slot stack).  At
+// the end each query's buffer becomes a workspace record, from which the
+// selection side finishes the block top-k and takes the row top-k.
 // Every mbarrier wait is bounded by a clock limit; a wait that runs out sets a
 // device error word (read by dsa_indexer_status) and the CTA winds down.
 
@@ -29,7 +37,7 @@
 #include <stdint.h>
 #include <string.h>
 
-#include "dsa_select.h"
+#include "dsa_internal.h"
 
 namespace {
 
@@ -66,6 +74,9 @@ constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kN 
                             ((uint32_t)(kM >> 4) << 24);
 
 __device__ int g_indexer_error;
+// Set by the first wait of this CTA that gives up; the CTA's later waits then
+// fail at once (an error left by an earlier launch does not affect this one).
+__shared__ int s_abort;
 
 struct IdxParams {
   const float* k_scale;
@@ -76,7 +87,15 @@ struct IdxParams {
   int64_t ld;
   int32_t T;
   int32_t S;
+  // fused selection (kFused): per-query streaming block top-Kb state is dumped
+  // to ws + t * ws_stride bytes
+  uint8_t* ws;
+  int64_t ws_stride;
+  int32_t B;       // block size, a power of two <= 8
+  int32_t log2B;
+  int32_t Kb;      // <= kFusedMaxKb
 };
+
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -107,14 +126,20 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity; false (and the error word set)
-// when it has not completed within kWaitCycles.
+// when it has not completed within kWaitCycles.  Once a wait of the CTA has
+// given up, its later waits fail at once, so warps that meet at named
+// barriers still walk their loops to the end in bounded time.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  if (*(volatile int*)&s_abort) return false;
   const long long t0 = clock64();
   while (!mbar_try(bar, parity)) {
     if (clock64() - t0 > kWaitCycles) {
+      *(volatile int*)&s_abort = 1;
       atomicExch(&g_indexer_error, 1);
       return false;
     }
+    if (*(volatile int*)&s_abort) return false;
   }
   return true;
 }
@@ -154,8 +179,24 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
+// 32 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+        "=r"(r[30]), "=r"(r[31])
+      : "r"(addr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // Dynamic shared memory, from a 1024-aligned base:
 //   Q tile [256 x 128 B] | K ring [4 x 128 x 128 B] | mbarriers | TMEM address | w [4 x 64] f32
+//   | (fused only) per-query streaming state x 4
 constexpr int kOffK = kTileQ;
 constexpr int kOffBar = kOffK + kStages * kTileK;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
@@ -164,9 +205,109 @@ constexpr int kOffW = (kOffTmem + 4 + 15) & ~15;
 constexpr int kSmemUsed = kOffW + kQueriesPerCta * kHeads * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024-byte alignment
 
+// Per-query streaming state of the fused variant:
+//   comp[cap] u64 (0 = free slot) | temp[cap] u64 (compaction scratch) |
+//   vals[cap * 8] f32 (the slot's block values) | freeq[cap] u16 (free slots) |
+//   last[8] f32 (the last live block's values) | insertion counter i32 | tau u64 | scan[4] i32
+constexpr int kQsComp = 0;
+constexpr int kQsTemp = kQsComp + kFusedCap * 8;
+constexpr int kQsVals = kQsTemp + kFusedCap * 8;
+constexpr int kQsFree = kQsVals + kFusedCap * kFusedMaxB * 4;
+constexpr int kQsLast = kQsFree + kFusedCap * 2;
+constexpr int kQsCnt = kQsLast + kFusedMaxB * 4;
+constexpr int kQsTau = kQsCnt + 8;
+constexpr int kQsScan = kQsTau + 8;
+constexpr int kQsBytes = (kQsScan + 16 + 127) & ~127;
+constexpr int kOffQs = (kSmemUsed + 127) & ~127;
+constexpr int kSmemFused = kOffQs + kQueriesPerCta * kQsBytes + 1024;
+
+__device__ __forceinline__ uint32_t okey(uint32_t u) { return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u); }
+__device__ __forceinline__ uint64_t ocomp(uint32_t key, uint32_t idx) {
+  return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - idx);
+}
+__device__ __forceinline__ uint32_t lanemask_lt_u() {
+  uint32_t m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+// Barrier of one query's four epilogue warps (ids 1..4; 0 is __syncthreads).
+__device__ __forceinline__ void group_bar(int q) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "r"(128) : "memory");
+}
+// The same barrier, returning whether any of the 128 threads passed true.
+__device__ __forceinline__ bool group_any(int q, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
+      " bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(1 + q), "r"(128)
+      : "memory");
+  return r != 0;
+}
+
+// Keep the Kb best entries of a query's buffer: an ascending bitonic sort of a
+// copy gives the Kb-th best X; entries below X are freed in place (values stay
+// in their slots) and the free-slot stack is rebuilt in slot order.  Called by
+// the query's 128 epilogue threads (lt = 0..127).
+__device__ __noinline__ void fused_compact(uint8_t* qs, int q, int lt, int Kb) {
+  uint64_t* comp = reinterpret_cast<uint64_t*>(qs + kQsComp);
+  uint64_t* temp = reinterpret_cast<uint64_t*>(qs + kQsTemp);
+  uint16_t* freeq = reinterpret_cast<uint16_t*>(qs + kQsFree);
+  int* cnt = reinterpret_cast<int*>(qs + kQsCnt);
+  uint64_t* tau = reinterpret_cast<uint64_t*>(qs + kQsTau);
+  int* scan = reinterpret_cast<int*>(qs + kQsScan);
+  for (int i = lt; i < kFusedCap; i += 128) temp[i] = comp[i];
+  group_bar(q);
+  for (int k = 2; k <= kFusedCap; k <<= 1) {
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = lt; i < kFusedCap; i += 128) {
+        const int ixj = i ^ j;
+        if (ixj > i) {
+          const uint64_t x = temp[i], y = temp[ixj];
+          if ((x > y) == ((i & k) == 0)) {
+            temp[i] = y;
+            temp[ixj] = x;
+          }
+        }
+      }
+      group_bar(q);
+    }
+  }
+  const uint64_t X = temp[kFusedCap - Kb];  // the Kb-th largest
+  for (int i = lt; i < kFusedCap; i += 128)
+    if (comp[i] < X) comp[i] = 0;
+  group_bar(q);
+  // free slots, ascending: 4 consecutive slots per thread, prefix over 128 threads
+  constexpr int kPer = kFusedCap / 128;
+  int c = 0;
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) c += comp[kPer * lt + i] == 0;
+  const int lane = lt & 31, wq = lt >> 5;
+  int incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scan[wq] = incl;
+  group_bar(q);
+  int pos = incl - c;
+  for (int w = 0; w < wq; ++w) pos += scan[w];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i)
+    if (comp[kPer * lt + i] == 0) freeq[pos++] = (uint16_t)(kPer * lt + i);
+  if (lt == 0) {
+    cnt[0] = 0;
+    *tau = X;
+  }
+  group_bar(q);
+}
+
+template <bool kFused>
 __global__ void __launch_bounds__(kThreads, 1)
-    indexer_logits_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                          const IdxParams p) {
+    indexer_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const IdxParams p) {
   extern __shared__ uint8_t dyn_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sq = base;
@@ -195,9 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       khi = max(khi, s1);
     }
   }
+  if (kFused && khi > 0) klo = 0;  // the fused form has start 0: blocks align with tiles
   const int ntiles = khi > klo ? (int)((khi - klo + kM - 1) / kM) : 0;
 
   if (threadIdx.x == 0) {
+    s_abort = 0;
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
@@ -213,6 +356,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = i / kHeads;
     ws[i] = q < nq ? p.w[(int64_t)(t0 + q) * kHeads + (i % kHeads)] : 0.f;
   }
+  if (kFused) {
+    for (int i = threadIdx.x; i < kQueriesPerCta * kFusedCap; i += kThreads) {
+      uint8_t* qs = base + kOffQs + (i / kFusedCap) * kQsBytes;
+      reinterpret_cast<uint64_t*>(qs + kQsComp)[i % kFusedCap] = 0;
+      reinterpret_cast<uint16_t*>(qs + kQsFree)[i % kFusedCap] = (uint16_t)(i % kFusedCap);
+    }
+    if (threadIdx.x < kQueriesPerCta) {
+      uint8_t* qs = base + kOffQs + threadIdx.x * kQsBytes;
+      reinterpret_cast<int*>(qs + kQsCnt)[0] = 0;
+      *reinterpret_cast<uint64_t*>(qs + kQsTau) = 0;
+    }
+  }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols));
@@ -223,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (ntiles > 0) {
-    if (warp == 0 && lane == 0) {
+  if (warp == 0 && lane == 0) {
+    if (ntiles > 0) {
       // TMA producer
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tk) : "memory");
@@ -236,108 +391,161 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_expect_tx(&full[st], kTileK + (i == 0 ? kStarveBytes : 0u));
         tma_load_2d(&tk, &full[st], sk + st * kTileK, 0, (int)(klo + (int64_t)i * kM));
       }
-    } else if (warp == 1 && lane == 0) {
-      // MMA issuer
-      if (mbar_wait(qbar, 0)) {
-        const uint64_t bdesc = sdesc_sw128(sq);
-        for (int i = 0; i < ntiles; ++i) {
-          const int st = i % kStages;
-          const int a = i & 1;
-          if (i >= 2 && !mbar_wait(&acce[a], ((i >> 1) & 1) ^ 1)) break;
-          if (!mbar_wait(&full[st], (i / kStages) & 1)) break;
-          tc_fence_after();
-          const uint64_t adesc = sdesc_sw128(sk + st * kTileK);
-          const uint32_t d = tmem + (uint32_t)(a * kN);
-#pragma unroll
-          for (int kk = 0; kk < kDim / kKStep; ++kk) {
-            // advance both start addresses by kk * 32 bytes inside the swizzled rows
-            umma_f8(d, adesc + (uint64_t)((kk * kKStep) >> 4), bdesc + (uint64_t)((kk * kKStep) >> 4), kk > 0);
-          }
-          umma_commit(&empty[st]);
-          umma_commit(&accf[a]);
-        }
-      }
-    } else if (warp >= 2) {
-      // epilogue: thread = key row m of the tile (TMEM lane); warp % 4 picks the
-      // lane quarter, the warps of a quarter split the four queries
-      constexpr int kQueriesPerWarp = kQueriesPerCta * 4 / kEpiWarps;
-      const int sub = warp & 3;
-      const int q0 = ((warp - 2) >> 2) * kQueriesPerWarp;
-      const int m = sub * 32 + lane;
-      const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
-      const float4* w4 = reinterpret_cast<const float4*>(ws);
-      // this warp's queries' live spans, read once
-      int64_t qs0[kQueriesPerWarp], qs1[kQueriesPerWarp];
-#pragma unroll
-      for (int j = 0; j < kQueriesPerWarp; ++j) {
-        const int q = q0 + j;
-        qs0[j] = 0;
-        qs1[j] = 0;
-        if (q < nq) {
-          const int t = t0 + q;
-          const int64_t a0 = p.starts ? (int64_t)p.starts[t] : 0;
-          qs0[j] = a0 > 0 ? a0 : 0;
-          qs1[j] = min((int64_t)p.ends[t], (int64_t)p.S);
-        }
-      }
-      int64_t s = klo + m;
-      float ksc = s < khi ? p.k_scale[s] : 0.f;
-      for (int i = 0; i < ntiles; ++i, s += kM) {
+    }
+  } else if (warp == 1 && lane == 0) {
+    // MMA issuer
+    if (ntiles > 0 && mbar_wait(qbar, 0)) {
+      const uint64_t bdesc = sdesc_sw128(sq);
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i % kStages;
         const int a = i & 1;
-        // the next tile's key scale is read while this tile is reduced
-        const int64_t sn = s + kM;
-        const float ksc_next = sn < khi ? p.k_scale[sn] : 0.f;
-        if (!mbar_wait(&accf[a], (i >> 1) & 1)) break;
+        if (i >= 2 && !mbar_wait(&acce[a], ((i >> 1) & 1) ^ 1)) break;
+        if (!mbar_wait(&full[st], (i / kStages) & 1)) break;
         tc_fence_after();
-#pragma unroll 1
-        for (int q = q0; q < q0 + kQueriesPerWarp; ++q) {
-          uint32_t r0[32], r1[32];
-          const uint32_t col = lane_addr + (uint32_t)(a * kN + q * kHeads);
-          asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-              "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-              : "=r"(r0[0]), "=r"(r0[1]), "=r"(r0[2]), "=r"(r0[3]), "=r"(r0[4]), "=r"(r0[5]), "=r"(r0[6]),
-                "=r"(r0[7]), "=r"(r0[8]), "=r"(r0[9]), "=r"(r0[10]), "=r"(r0[11]), "=r"(r0[12]), "=r"(r0[13]),
-                "=r"(r0[14]), "=r"(r0[15]), "=r"(r0[16]), "=r"(r0[17]), "=r"(r0[18]), "=r"(r0[19]),
-                "=r"(r0[20]), "=r"(r0[21]), "=r"(r0[22]), "=r"(r0[23]), "=r"(r0[24]), "=r"(r0[25]),
-                "=r"(r0[26]), "=r"(r0[27]), "=r"(r0[28]), "=r"(r0[29]), "=r"(r0[30]), "=r"(r0[31])
-              : "r"(col));
-          asm volatile(
-              "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-              "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-              : "=r"(r1[0]), "=r"(r1[1]), "=r"(r1[2]), "=r"(r1[3]), "=r"(r1[4]), "=r"(r1[5]), "=r"(r1[6]),
-                "=r"(r1[7]), "=r"(r1[8]), "=r"(r1[9]), "=r"(r1[10]), "=r"(r1[11]), "=r"(r1[12]), "=r"(r1[13]),
-                "=r"(r1[14]), "=r"(r1[15]), "=r"(r1[16]), "=r"(r1[17]), "=r"(r1[18]), "=r"(r1[19]),
-                "=r"(r1[20]), "=r"(r1[21]), "=r"(r1[22]), "=r"(r1[23]), "=r"(r1[24]), "=r"(r1[25]),
-                "=r"(r1[26]), "=r"(r1[27]), "=r"(r1[28]), "=r"(r1[29]), "=r"(r1[30]), "=r"(r1[31])
-              : "r"(col + 32u));
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-          // four independent partial sums (one per float4 lane) keep the FMA
-          // dependency chains short
-          float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        const uint64_t adesc = sdesc_sw128(sk + st * kTileK);
+        const uint32_t d = tmem + (uint32_t)(a * kN);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 wv = w4[q * (kHeads / 4) + j];
-            acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r0[4 * j + 0]), 0.f), acc0);
-            acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r0[4 * j + 1]), 0.f), acc1);
-            acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r0[4 * j + 2]), 0.f), acc2);
-            acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r0[4 * j + 3]), 0.f), acc3);
-          }
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float4 wv = w4[q * (kHeads / 4) + 8 + j];
-            acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r1[4 * j + 0]), 0.f), acc0);
-            acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r1[4 * j + 1]), 0.f), acc1);
-            acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r1[4 * j + 2]), 0.f), acc2);
-            acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r1[4 * j + 3]), 0.f), acc3);
-          }
-          const float acc = (acc0 + acc1) + (acc2 + acc3);
-          const int j = q - q0;
-          if (s >= qs0[j] && s < qs1[j]) p.out[(int64_t)(t0 + q) * p.ld + s] = acc * ksc;
+        for (int kk = 0; kk < kDim / kKStep; ++kk) {
+          // advance both start addresses by kk * 32 bytes inside the swizzled rows
+          umma_f8(d, adesc + (uint64_t)((kk * kKStep) >> 4), bdesc + (uint64_t)((kk * kKStep) >> 4), kk > 0);
         }
-        tc_fence_before();
-        mbar_arrive(&acce[a]);
-        ksc = ksc_next;
+        umma_commit(&empty[st]);
+        umma_commit(&accf[a]);
+      }
+    }
+  } else if (warp >= 2) {
+    // epilogue: thread = key row m of the tile (TMEM lane); warp % 4 picks the
+    // lane quarter, the four warps of a quarter group each own one query
+    static_assert(kEpiWarps == 4 * kQueriesPerCta, "one query per epilogue warp");
+    const int sub = warp & 3;
+    const int q = (warp - 2) >> 2;
+    const int m = sub * 32 + lane;
+    const int lt = ((warp - 2) & 3) * 32 + lane;  // thread index within the query's group
+    const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
+    const float4* w4 = reinterpret_cast<const float4*>(ws);
+    // this warp's query's live span, read once
+    int64_t qs0 = 0, qs1 = 0;
+    if (q < nq) {
+      const int t = t0 + q;
+      const int64_t a0 = (!kFused && p.starts) ? (int64_t)p.starts[t] : 0;
+      qs0 = a0 > 0 ? a0 : 0;
+      qs1 = min((int64_t)p.ends[t], (int64_t)p.S);
+    }
+    uint8_t* qst = base + kOffQs + q * kQsBytes;
+    const int nbq = (kFused && qs1 > 0) ? (int)((qs1 + p.B - 1) >> p.log2B) : 0;
+    uint64_t tau = 0;
+    int valid = 0;   // entries kept by the last compaction (0 or Kb)
+    int used = 0;    // this warp's latest view of the insertions since then
+    int64_t s = klo + m;
+    float ksc = s < khi ? p.k_scale[s] : 0.f;
+    for (int i = 0; i < ntiles; ++i, s += kM) {
+      const int a = i & 1;
+      // the next tile's key scale is read while this tile is reduced
+      const int64_t sn = s + kM;
+      const float ksc_next = sn < khi ? p.k_scale[sn] : 0.f;
+      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&accf[a], (i >> 1) & 1));
+      if (ok) {
+        tc_fence_after();
+        uint32_t r0[32], r1[32];
+        const uint32_t col = lane_addr + (uint32_t)(a * kN + q * kHeads);
+        // heads 0-31 and 32-63; the fused form reads the second half after
+        // reducing the first, so both halves never hold registers together
+        tmem_ld32(col, r0);
+        if constexpr (!kFused) tmem_ld32(col + 32u, r1);
+        tmem_wait_ld();
+        // four independent partial sums (one per float4 lane) keep the FMA
+        // dependency chains short; the order of the sums is the same in both
+        // forms, so their values are bit-identical
+        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 wv = w4[q * (kHeads / 4) + j];
+          acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r0[4 * j + 0]), 0.f), acc0);
+          acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r0[4 * j + 1]), 0.f), acc1);
+          acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r0[4 * j + 2]), 0.f), acc2);
+          acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r0[4 * j + 3]), 0.f), acc3);
+        }
+        if constexpr (kFused) {
+          tmem_ld32(col + 32u, r1);
+          tmem_wait_ld();
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const float4 wv = w4[q * (kHeads / 4) + 8 + j];
+          acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r1[4 * j + 0]), 0.f), acc0);
+          acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r1[4 * j + 1]), 0.f), acc1);
+          acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r1[4 * j + 2]), 0.f), acc2);
+          acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r1[4 * j + 3]), 0.f), acc3);
+        }
+        const float v = ((acc0 + acc1) + (acc2 + acc3)) * ksc;
+        if constexpr (!kFused) {
+          if (s >= qs0 && s < qs1) p.out[(int64_t)(t0 + q) * p.ld + s] = v;
+        } else {
+          // block maxima over B consecutive keys (lanes), then the query's
+          // streaming top-Kb: a slot per winning block, its B values beside it
+          const int Bq = p.B;
+          uint32_t mx = s < qs1 ? okey(__float_as_uint(v)) : 0u;
+          for (int o = 1; o < Bq; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+          const int jb = (int)(s >> p.log2B);
+          const uint64_t c = ocomp(mx, (uint32_t)jb);
+          const bool ins = ((lane & (Bq - 1)) == 0) && jb < nbq && c > tau;
+          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ins);
+          if (bal) {
+            int* cnt = reinterpret_cast<int*>(qst + kQsCnt);
+            const int leader = __ffs(bal) - 1;
+            int basei = 0;
+            if (lane == leader) basei = atomicAdd(&cnt[0], __popc(bal));
+            basei = __shfl_sync(0xFFFFFFFFu, basei, leader);
+            used = basei + __popc(bal);
+            int slot = -1;
+            if (ins) {
+              const int idx = basei + __popc(bal & lanemask_lt_u());
+              if (idx < kFusedCap - valid) {
+                slot = reinterpret_cast<const uint16_t*>(qst + kQsFree)[idx];
+                reinterpret_cast<uint64_t*>(qst + kQsComp)[slot] = c;
+              } else {
+                atomicExch(&g_indexer_error, 2);  // unreachable: the capacity check keeps a tile's room
+              }
+            }
+            const int bslot = __shfl_sync(0xFFFFFFFFu, slot, lane & ~(Bq - 1));
+            if (bslot >= 0) reinterpret_cast<float*>(qst + kQsVals)[bslot * Bq + (lane & (Bq - 1))] = v;
+          }
+          if (jb == nbq - 1) reinterpret_cast<float*>(qst + kQsLast)[lane & (Bq - 1)] = v;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&acce[a]);
+      ksc = ksc_next;
+      if constexpr (kFused) {
+        // Capacity check, one reducing barrier per tile.  The shared counter
+        // is only ever raised by atomics, so the warp whose atomic came last
+        // saw the full count and the OR over the group is exact: all four
+        // warps take the same branch.
+        // A tile inserts at most 128 / B blocks per query; compacting once
+        // the buffer could not take another tile keeps every insertion in
+        // bounds.
+        if (i + 1 < ntiles && group_any(q, valid + used > kFusedCap - (kM >> p.log2B))) {
+          fused_compact(qst, q, lt, p.Kb);
+          tau = *reinterpret_cast<const uint64_t*>(qst + kQsTau);
+          valid = p.Kb;
+          used = 0;
+        }
+      }
+    }
+    if constexpr (kFused) {
+      // the query's record for the finishing kernel
+      group_bar(q);
+      if (q < nq) {
+        uint8_t* rec = p.ws + (int64_t)(t0 + q) * p.ws_stride;
+        const uint64_t* comp = reinterpret_cast<const uint64_t*>(qst + kQsComp);
+        const float* vals = reinterpret_cast<const float*>(qst + kQsVals);
+        uint64_t* rc = reinterpret_cast<uint64_t*>(rec);
+        float* rv = reinterpret_cast<float*>(rec + (int64_t)kFusedCap * 8);
+        float* rl = rv + (int64_t)kFusedCap * p.B;
+        const bool empty_row = ntiles == 0 || nbq == 0;
+        for (int i = lt; i < kFusedCap; i += 128) rc[i] = empty_row ? 0ull : comp[i];
+        for (int i = lt; i < kFusedCap * p.B; i += 128) rv[i] = vals[i];
+        if (lt < p.B) rl[lt] = reinterpret_cast<const float*>(qst + kQsLast)[lt];
       }
     }
   }
@@ -375,23 +583,31 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint32_t box_ro
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-}  // namespace
-
-extern "C" {
-
-int dsa_indexer_logits(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const float* k_scale,
-                       const float* w, const int32_t* starts, const int32_t* ends, float* logits,
-                       struct CUstream_st* stream) {
+// Checks shared by both entry points; DSA_OK with `*empty` set when there is
+// nothing to launch.
+int check_cfg(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const float* k_scale,
+              const float* w, const int32_t* ends, bool* empty) {
+  *empty = false;
   if (!cfg) return DSA_ERR_INVALID_ARG;
-  if (cfg->queries < 0 || cfg->keys < 0 || cfg->out_stride < cfg->keys) return DSA_ERR_INVALID_ARG;
+  if (cfg->queries < 0 || cfg->keys < 0) return DSA_ERR_INVALID_ARG;
   if (cfg->heads != kHeads || cfg->head_dim != kDim) return DSA_ERR_UNSUPPORTED;
   if ((int64_t)cfg->queries * kHeads > INT32_MAX) return DSA_ERR_UNSUPPORTED;
-  if (cfg->queries == 0 || cfg->keys == 0) return DSA_OK;
-  if (!q || !k || !k_scale || !w || !ends || !logits) return DSA_ERR_INVALID_ARG;
-  if ((((uintptr_t)q) & 15u) || (((uintptr_t)k) & 15u) || (((uintptr_t)logits) & 3u)) return DSA_ERR_INVALID_ARG;
+  if (cfg->queries == 0 || cfg->keys == 0) {
+    *empty = true;
+    return DSA_OK;
+  }
+  if (!q || !k || !k_scale || !w || !ends) return DSA_ERR_INVALID_ARG;
+  if ((((uintptr_t)q) & 15u) || (((uintptr_t)k) & 15u)) return DSA_ERR_INVALID_ARG;
+  return DSA_OK;
+}
+
+template <bool kFused>
+int launch(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const IdxParams& P,
+           cudaStream_t stream) {
+  constexpr int smem = kFused ? kSmemFused : kSmemBytes;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(indexer_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+    if (cudaFuncSetAttribute(indexer_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess) {
       cudaGetLastError();
       return DSA_ERR_CUDA;
@@ -401,7 +617,26 @@ int dsa_indexer_logits(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8
   CUtensorMap tq, tk;
   if (!make_map(&tq, q, (uint64_t)cfg->queries * kHeads, kN) || !make_map(&tk, k, (uint64_t)cfg->keys, kM))
     return DSA_ERR_CUDA;
+  const int grid = (cfg->queries + kQueriesPerCta - 1) / kQueriesPerCta;
+  indexer_kernel<kFused><<<grid, kThreads, smem, stream>>>(tq, tk, P);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsa_indexer_logits(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const float* k_scale,
+                       const float* w, const int32_t* starts, const int32_t* ends, float* logits,
+                       struct CUstream_st* stream) {
+  bool empty = false;
+  int st = check_cfg(cfg, q, k, k_scale, w, ends, &empty);
+  if (st != DSA_OK) return st;
+  if (cfg->out_stride < cfg->keys) return DSA_ERR_INVALID_ARG;
+  if (empty) return DSA_OK;
+  if (!logits || (((uintptr_t)logits) & 3u)) return DSA_ERR_INVALID_ARG;
   IdxParams P;
+  memset(&P, 0, sizeof(P));
   P.k_scale = k_scale;
   P.w = w;
   P.starts = starts;
@@ -410,9 +645,54 @@ int dsa_indexer_logits(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8
   P.ld = cfg->out_stride;
   P.T = cfg->queries;
   P.S = cfg->keys;
-  const int grid = (cfg->queries + kQueriesPerCta - 1) / kQueriesPerCta;
-  indexer_logits_kernel<<<grid, kThreads, kSmemBytes, (cudaStream_t)stream>>>(tq, tk, P);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  return launch<false>(cfg, q, k, P, (cudaStream_t)stream);
+}
+
+int dsa_indexer_select_workspace(const dsa_select_plan* plan, size_t* bytes) {
+  if (!bytes) return DSA_ERR_INVALID_ARG;
+  *bytes = 0;
+  int32_t rows = 0, B = 0, Kb = 0;
+  int64_t width = 0;
+  const int st = dsa_fused_shape(plan, &rows, &width, &B, &Kb);
+  if (st != DSA_OK) return st;
+  *bytes = (size_t)rows * (size_t)fused_record_bytes(B);
+  return DSA_OK;
+}
+
+int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, const uint8_t* q,
+                       const uint8_t* k, const float* k_scale, const float* w, const int32_t* ends,
+                       void* workspace, size_t workspace_bytes, int32_t* cand, int32_t* topk,
+                       struct CUstream_st* stream) {
+  int32_t rows = 0, B = 0, Kb = 0;
+  int64_t width = 0;
+  int st = dsa_fused_shape(plan, &rows, &width, &B, &Kb);
+  if (st != DSA_OK) return st;
+  bool empty = false;
+  st = check_cfg(cfg, q, k, k_scale, w, ends, &empty);
+  if (st != DSA_OK) return st;
+  if (cfg->queries != rows || (int64_t)cfg->keys != width) return DSA_ERR_INVALID_ARG;
+  if (rows == 0) return DSA_OK;  // keys == width >= 1, so only an empty batch is empty
+  const int64_t rec = fused_record_bytes(B);
+  if (!workspace || (((uintptr_t)workspace) & 15u) || workspace_bytes < (size_t)rows * (size_t)rec ||
+      !cand || !topk)
+    return DSA_ERR_INVALID_ARG;
+  IdxParams P;
+  memset(&P, 0, sizeof(P));
+  P.k_scale = k_scale;
+  P.w = w;
+  P.starts = nullptr;
+  P.ends = ends;
+  P.T = cfg->queries;
+  P.S = cfg->keys;
+  P.ws = static_cast<uint8_t*>(workspace);
+  P.ws_stride = rec;
+  P.B = B;
+  P.log2B = B == 1 ? 0 : B == 2 ? 1 : B == 4 ? 2 : 3;
+  P.Kb = Kb;
+  st = launch<true>(cfg, q, k, P, (cudaStream_t)stream);
+  if (st != DSA_OK) return st;
+  return dsa_fused_finish(plan, static_cast<const uint8_t*>(workspace), rec, ends, cand, topk,
+                          (cudaStream_t)stream);
 }
 
 int dsa_indexer_status(void) {

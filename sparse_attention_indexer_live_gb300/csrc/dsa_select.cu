@@ -33,7 +33,7 @@
 
 #include <new>
 
-#include "dsa_select.h"
+#include "dsa_internal.h"
 
 namespace {
 
@@ -592,13 +592,26 @@ __device__ void write_mask(const Params& p, float* rowp, const Row& R, const uin
   }
 }
 
+// Values read from the logits row (after the mask, kept columns are intact).
+struct RowValues {
+  const float* rowp;
+  int64_t cs;
+  __device__ __forceinline__ void prep(const int32_t*, int) {}
+  __device__ __forceinline__ float load(int, int64_t c) const { return __ldcg(rowp + c * cs); }
+};
+
 // ---------------------------------------------------------------------------
 // Step 5, candidate mode: row top-k from the kept blocks (bitmap) and the
 // edge flag, on logits already masked with them.  `region` is shared memory
 // laid out as comp[cand_cap] u64 | aux[cand_cap] u64 | kb[Kb+1] i32 |
 // list_a[max(K, cand_cap)] i32 | list_b[K] i32.
 
-__device__ void row_topk_kept(const Params& p, const float* rowp, const Row& R, int r, const uint32_t* bitmap,
+//
+// `src` supplies the values of kept columns: src.prep(kb, nkb) runs once the
+// kept block ids kb[0 .. nkb) (ascending) are known, src.load(j, c) returns
+// column c, a column of block kb[j] (j = -1: the block is not given).
+template <class Src>
+__device__ void row_topk_kept(const Params& p, Src& src, const Row& R, int r, const uint32_t* bitmap,
                               bool edge, uint8_t* region, Shared& sh) {
   const int K = p.K;
   int32_t* out = p.topk + (int64_t)r * K;
@@ -616,10 +629,10 @@ __device__ void row_topk_kept(const Params& p, const float* rowp, const Row& R, 
   int32_t* lb = la + (K > cc ? K : cc);
   const int64_t W = p.width;
   const int64_t ec = s + L;
-  const int64_t cs = p.col_stride;
   const int B = p.B;
 
   const int nkb = min(enumerate_bits(bitmap, R.nb, kb, p.Kb + 1, sh), p.Kb + 1);
+  src.prep(kb, nkb);
   // the edge column W-1 is a candidate of its own when its block is not kept
   const bool edge_extra = edge && ec == W && (W - 1) >= s && !bit_set(bitmap, R.nb - 1);
   const int nslots = nkb * B + (edge_extra ? 1 : 0);
@@ -628,14 +641,17 @@ __device__ void row_topk_kept(const Params& p, const float* rowp, const Row& R, 
   int my_valid = 0, my_hi = 0, my_eq = 0;
   for (int i = threadIdx.x; i < nslots; i += kThreads) {
     int64_t c;
+    int j;
     if (i < nkb * B) {
-      c = s + (int64_t)kb[i / B] * B + (i % B);
+      j = i / B;
+      c = s + (int64_t)kb[j] * B + (i % B);
     } else {
+      j = -1;
       c = W - 1;
     }
     uint64_t v = 0;
     if (c < ec) {
-      const uint32_t key = order_key(__float_as_uint(__ldcg(rowp + c * cs)));
+      const uint32_t key = order_key(__float_as_uint(src.load(j, c)));
       v = compose(key, (uint32_t)c);
       ++my_valid;
       my_hi += key > kKeyNegInf;
@@ -685,7 +701,7 @@ __device__ void row_topk_kept(const Params& p, const float* rowp, const Row& R, 
         const int64_t c = c0 + k;
         if (c < ec) {
           const bool kept = bit_set(bitmap, (c - s) / B) || (edge_extra && c == W - 1);
-          if (!kept || __float_as_uint(__ldcg(rowp + c * cs)) == kNegInfBits) hits |= 1u << k;
+          if (!kept || __float_as_uint(src.load(-1, c)) == kNegInfBits) hits |= 1u << k;
         }
       }
       int tot;
@@ -847,8 +863,86 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   if (clustered) cg::this_cluster().sync();  // masks visible to the leader
   if (kTopK && rank == 0) {
     __syncthreads();
-    row_topk_kept(p, rowp, R, r, bitmap, edge, region, sh);
+    RowValues src{rowp, p.col_stride};
+    row_topk_kept(p, src, R, r, bitmap, edge, region, sh);
   }
+}
+
+// Values of the fused indexer selection, from one query's record (start 0):
+// the last live block from its own copy, every other kept block from the
+// streaming slot that holds it.
+struct RecordValues {
+  const uint64_t* comp;  // record: comp[kFusedCap]
+  const float* vals;     // record: vals[kFusedCap << log2B]
+  const float* last;     // record: last[B]
+  int32_t* kslot;        // shared: kslot[j] = slot of block kb[j]
+  const int32_t* kb;
+  int nkb;
+  int64_t last_block;    // n_b - 1
+  int log2B;
+  __device__ void prep(const int32_t* kb_, int nkb_) {
+    kb = kb_;
+    nkb = nkb_;
+    for (int j = threadIdx.x; j < nkb; j += kThreads) kslot[j] = 0;  // every read stays in the record
+    __syncthreads();
+    for (int i = threadIdx.x; i < kFusedCap; i += kThreads) {
+      const uint64_t c = __ldcg(comp + i);
+      if (c == 0) continue;
+      const int32_t b = (int32_t)comp_index(c);
+      const int j = lower_bound_i32(kb, nkb, b);
+      if (j < nkb && kb[j] == b) kslot[j] = i;
+    }
+    __syncthreads();
+  }
+  __device__ __forceinline__ float load(int j, int64_t c) const {
+    const int64_t b = c >> log2B;
+    const int o = (int)(c & ((1 << log2B) - 1));
+    if (b == last_block) return __ldcg(last + o);
+    if (j < 0) j = min(lower_bound_i32(kb, nkb, (int32_t)b), nkb - 1);  // kept blocks are all in kb
+    return __ldcg(vals + ((int64_t)kslot[j] << log2B) + o);
+  }
+};
+
+// Second launch of the fused indexer selection: one CTA per query takes the
+// non-empty slots of the query's record as its streaming buffer, finishes the
+// block top-k exactly as the select kernel does (padding blocks, pin, edge
+// flag, cand) and takes the row top-k from the kept blocks' values.  Nothing
+// is masked: there is no logits row.
+// Dynamic shared memory: bitmap[bitmap_words] u32 | keep[Kb] u64 |
+// kslot[Kb + 1] i32 | region (the larger of the buffer and the row top-k layout)
+__global__ void __launch_bounds__(kThreads, 2)
+    fused_finish_kernel(const Params p, const uint8_t* records, int64_t record_bytes) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ Shared sh;
+  const int r = blockIdx.x;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(dyn);
+  uint64_t* keep = reinterpret_cast<uint64_t*>(dyn + (((size_t)p.bitmap_words * 4 + 15) & ~(size_t)15));
+  int32_t* kslot = reinterpret_cast<int32_t*>(keep + p.Kb);
+  uint8_t* region = reinterpret_cast<uint8_t*>(kslot) + (((size_t)(p.Kb + 1) * 4 + 15) & ~(size_t)15);
+  uint64_t* buf = reinterpret_cast<uint64_t*>(region);
+  for (int i = threadIdx.x; i < p.bitmap_words; i += kThreads) bitmap[i] = 0;
+  if (threadIdx.x == 0) {
+    sh.cnt = 0;
+    sh.tau = 0;
+    sh.edge = 0;
+  }
+  const Row R = load_row(p, r);
+  const uint8_t* rec = records + (int64_t)r * record_bytes;
+  const uint64_t* comp = reinterpret_cast<const uint64_t*>(rec);
+  __syncthreads();
+  // only ids of live blocks can be in a record; anything else is ignored, so
+  // the bitmap stays in bounds whatever the workspace holds
+  for (int i0 = 0; i0 < kFusedCap; i0 += kThreads) {
+    const int i = i0 + threadIdx.x;
+    const uint64_t c = i < kFusedCap ? __ldcg(comp + i) : 0;
+    warp_append(c != 0 && comp_index(c) < (uint32_t)R.nb, c, buf, &sh.cnt, p.cap);
+  }
+  __syncthreads();
+  finish_block_topk(p, R, r, buf, keep, bitmap, sh);
+  const float* vals = reinterpret_cast<const float*>(rec + (int64_t)kFusedCap * 8);
+  RecordValues src{comp, vals, vals + ((int64_t)kFusedCap << p.log2B), kslot, nullptr, 0, (int64_t)R.nb - 1,
+                   p.log2B};
+  row_topk_kept(p, src, R, r, bitmap, sh.edge != 0, region, sh);
 }
 
 // Candidate-mode row top-k: rebuild the kept bitmap from cand.
@@ -875,7 +969,8 @@ __global__ void __launch_bounds__(kThreads, 2) topk_cand_kernel(const Params p) 
     }
   }
   __syncthreads();
-  row_topk_kept(p, rowp, R, r, bitmap, sh.edge != 0, region, sh);
+  RowValues src{rowp, p.col_stride};
+  row_topk_kept(p, src, R, r, bitmap, sh.edge != 0, region, sh);
 }
 
 // Ascending bitonic sort of a[0 .. n) in shared memory, n a power of two.
@@ -1041,6 +1136,7 @@ struct dsa_select_plan {
   size_t smem_select;
   size_t smem_topk_cand;
   size_t smem_topk_scan;
+  size_t smem_fused;  // fused indexer selection's finishing kernel; 0 = the plan cannot take that form
   int ctas_per_sm_select;
 };
 
@@ -1079,6 +1175,25 @@ struct Sizes {
   size_t select, cand, scan;
 };
 
+// Shared memory of the candidate-mode row top-k layout.
+size_t cand_layout_bytes(const Params& P) {
+  return align16((size_t)P.cand_cap * 16 + (size_t)(P.Kb + 1) * 4 +
+                 (size_t)(P.K > P.cand_cap ? P.K : P.cand_cap) * 4 + (size_t)P.K * 4);
+}
+
+// Shared memory of the fused form's finishing kernel, or 0 when the plan
+// cannot take the fused form (start 0, one row per bound, unit column stride,
+// a block that fits the producer's lane groups, Kb within its buffer).
+size_t fused_smem(const dsa_select_cfg* c, const Params& P) {
+  const int B = c->block_size;
+  if (c->has_starts || c->row_repeat != 1 || c->col_stride != 1) return 0;
+  if (!(B == 1 || B == 2 || B == 4 || B == 8) || c->block_topk > kFusedMaxKb) return 0;
+  const size_t buf = (size_t)(kFusedCap + P.Kb) * 8;
+  const size_t cl = cand_layout_bytes(P);
+  return align16((size_t)P.bitmap_words * 4) + align16((size_t)P.Kb * 8) + align16((size_t)(P.Kb + 1) * 4) +
+         (buf > cl ? buf : cl);
+}
+
 // Shared-memory sizes for a plan whose select kernel runs `split` CTAs per row
 // (the cluster leader's buffer must hold every CTA's top-Kb plus Kb padding).
 Sizes sizes_for(Params& P, int split) {
@@ -1088,9 +1203,7 @@ Sizes sizes_for(Params& P, int split) {
   if (cap < 4096) cap = 4096;
   cap = (cap + 255) & ~255;
   const size_t bitmap_bytes = align16((size_t)P.bitmap_words * 4);
-  const size_t cand_layout = align16((size_t)P.cand_cap * 16 + (size_t)(P.Kb + 1) * 4 +
-                                     (size_t)(P.K > P.cand_cap ? P.K : P.cand_cap) * 4 +
-                                     (size_t)P.K * 4);
+  const size_t cand_layout = cand_layout_bytes(P);
   // the region holds the larger of the streaming buffer and the row top-k
   // layout; let the buffer use all of it (longer epochs between barriers)
   const int cap_region = (int)((cand_layout / 8) & ~(size_t)255);
@@ -1264,6 +1377,13 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
       rc = DSA_ERR_CUDA;
     }
   }
+  size_t smem_f = rc == DSA_OK ? fused_smem(cfg, P) : 0;
+  if (smem_f && (smem_f + static_smem > (size_t)smem_optin ||
+                 cudaFuncSetAttribute(fused_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)smem_f) != cudaSuccess)) {
+    cudaGetLastError();
+    smem_f = 0;  // the plan still serves every other call
+  }
   if (prev >= 0 && prev != device) cudaSetDevice(prev);
   if (rc != DSA_OK) {
     cudaGetLastError();
@@ -1279,6 +1399,7 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
   pl->smem_select = z.select;
   pl->smem_topk_cand = z.cand;
   pl->smem_topk_scan = z.scan;
+  pl->smem_fused = smem_f;
   pl->ctas_per_sm_select = ctas;
   *plan = pl;
   if (workspace_bytes) *workspace_bytes = 0;
@@ -1393,3 +1514,28 @@ int dsa_combine_window(const dsa_select_plan* plan, const int32_t* starts, const
 }
 
 }  // extern "C"
+
+int dsa_fused_shape(const dsa_select_plan* plan, int32_t* rows, int64_t* width, int32_t* B, int32_t* Kb) {
+  if (!plan) return DSA_ERR_INVALID_ARG;
+  if (plan->smem_fused == 0) return DSA_ERR_UNSUPPORTED;
+  *rows = plan->cfg.rows;
+  *width = plan->cfg.width;
+  *B = plan->cfg.block_size;
+  *Kb = plan->cfg.block_topk;
+  return DSA_OK;
+}
+
+int dsa_fused_finish(const dsa_select_plan* plan, const uint8_t* records, int64_t record_bytes,
+                     const int32_t* ends, int32_t* cand, int32_t* topk, cudaStream_t stream) {
+  if (!plan || plan->smem_fused == 0) return DSA_ERR_UNSUPPORTED;
+  if (plan->cfg.rows == 0) return DSA_OK;
+  Params P = plan->base;
+  P.logits = nullptr;
+  P.starts = nullptr;
+  P.ends = ends;
+  P.cand = cand;
+  P.topk = topk;
+  P.cap = kFusedCap + P.Kb;
+  fused_finish_kernel<<<plan->cfg.rows, kThreads, plan->smem_fused, stream>>>(P, records, record_bytes);
+  return finish_launch(cudaSuccess);
+}

@@ -2,7 +2,8 @@
 build of the library (compile-time hooks, never in the product build) makes
 the first K stage's mbarrier expect one chunk more than its copy delivers, so
 the bounded waits run out; the kernel then winds down, dsa_indexer_status()
-reports DSA_ERR_TIMEOUT once, and the CUDA context stays usable."""
+reports DSA_ERR_TIMEOUT once, and the CUDA context stays usable.  The same
+holds for the fused producer + selection form."""
 import os
 import subprocess
 import sys
@@ -46,14 +47,28 @@ def test_bounded_wait_reports_timeout(tmp_path):
         torch.cuda.synchronize()
         first = dsa.dsa_indexer_status()
         second = dsa.dsa_indexer_status()
+        # the fused form: its epilogue warps meet at named barriers every tile,
+        # so after the first wait gives up they must still walk every tile
+        plan = dsa.dsa_select_init(rows=8, width=4096, block_size=8, block_topk=32, row_topk=64)
+        ws = torch.zeros(dsa.dsa_indexer_select_workspace(plan), dtype=torch.uint8, device=d)
+        cand = torch.empty((8, 33), dtype=torch.int32, device=d)
+        topk = torch.empty((8, 64), dtype=torch.int32, device=d)
+        dsa.dsa_indexer_select(plan, torch.from_numpy(q).to(d), torch.from_numpy(k).to(d),
+                               torch.from_numpy(ks).to(d), torch.from_numpy(w).to(d),
+                               torch.from_numpy(en).to(d), ws, cand, topk)
+        torch.cuda.synchronize()
+        third = dsa.dsa_indexer_status()
+        fourth = dsa.dsa_indexer_status()
         alive = float(torch.ones(1024, device=d).sum().item())
-        print(first, second, alive)
+        print(first, second, third, fourth, alive)
     """)
     res = subprocess.run([sys.executable, "-c", script], capture_output=True, text=True,
                          timeout=300)
     assert res.returncode == 0, res.stderr[-2000:]
-    first, second, alive = res.stdout.split()[-3:]
+    first, second, third, fourth, alive = res.stdout.split()[-5:]
     import sparse_attention_indexer_live_gb300 as dsa
     assert int(first) == dsa.DSA_ERR_TIMEOUT
     assert int(second) == dsa.DSA_OK       # reported once, then cleared
+    assert int(third) == dsa.DSA_ERR_TIMEOUT  # the fused form winds down the same way
+    assert int(fourth) == dsa.DSA_OK
     assert float(alive) == 1024.0          # the context is still usable
