@@ -16,9 +16,11 @@
 //               of 128B-swizzled shared memory (cp.async.bulk.tensor + mbarrier)
 //   warp 1      tcgen05.mma issuer (kind::f8f6f4, fp32 accumulator in TMEM,
 //               two 256-column accumulators so MMA and epilogue overlap)
-//   warps 2-17  epilogue: four warps per TMEM lane quarter, each reading its key
+//   warps 2-3   idle (they complete the control warpgroup for setmaxnreg)
+//   warps 4-19  epilogue: four warps per TMEM lane quarter, each reading its key
 //               row's 64 columns of one query with tcgen05.ld, weighted ReLU sum
-//               over the heads, coalesced fp32 stores of the live span
+//               over the heads (weights in registers, packed FMAs), coalesced
+//               fp32 stores of the live span
 // Fused form (dsa_indexer_select): the same epilogue values, never stored.
 // Each query's four warps reduce them to block maxima (shuffles across B
 // lanes) and keep a streaming top-Kb of blocks in shared memory: a slot per
@@ -51,7 +53,19 @@ constexpr int kStages = 4;
 constexpr int kTileK = kM * kDim;              // 16 KB
 constexpr int kTileQ = kN * kDim;              // 32 KB
 constexpr int kEpiWarps = 16;                  // a multiple of 4: warps per TMEM lane quarter x 4
-constexpr int kThreads = (2 + kEpiWarps) * 32; // TMA warp, MMA warp, epilogue warps
+constexpr int kCtrlWarps = 4;                  // one warpgroup: TMA warp, MMA warp, two idle warps
+constexpr int kThreads = (kCtrlWarps + kEpiWarps) * 32;
+// Register split (setmaxnreg): the launch gives every thread 96 registers (five
+// warps per SM sub-partition); the control warpgroup drops to 40 so that the
+// epilogue warpgroups can hold 104 -- a query's 64 head weights stay in
+// registers instead of being re-read from shared memory every tile (those
+// reads shared the load/store data path with the TMEM loads, its bottleneck).
+// 128 x 40 + 512 x 104 = 58,368 <= 640 x 96 = 61,440 registers.
+constexpr int kLaunchRegs = 96;
+constexpr int kCtrlRegs = 40;
+constexpr int kEpiRegs = 104;
+static_assert(kCtrlWarps * 32 * kCtrlRegs + kEpiWarps * 32 * kEpiRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;            // two fp32 accumulators of 256 columns
 // Bounded waits.  A separate test build (tests/test_gpu_indexer_timeout.py)
 // defines DSA_INDEXER_TEST_WAIT_CYCLES to shorten the limit and
@@ -179,20 +193,32 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t addr, uint32_t (&r)[32]) {
+// 16 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t addr, uint32_t (&r)[16]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-        "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-        "=r"(r[30]), "=r"(r[31])
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(addr));
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Two fp32 lanes per instruction (packed FMA): each lane is an ordinary
+// round-to-nearest fused multiply-add.
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
 
 // Dynamic shared memory, from a 1024-aligned base:
 //   Q tile [256 x 128 B] | K ring [4 x 128 x 128 B] | mbarriers | TMEM address | w [4 x 64] f32
@@ -378,51 +404,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    if (ntiles > 0) {
-      // TMA producer
-      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
-      asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tk) : "memory");
-      mbar_expect_tx(qbar, kTileQ);
-      tma_load_2d(&tq, qbar, sq, 0, t0 * kHeads);
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kStages;
-        if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) break;
-        mbar_expect_tx(&full[st], kTileK + (i == 0 ? kStarveBytes : 0u));
-        tma_load_2d(&tk, &full[st], sk + st * kTileK, 0, (int)(klo + (int64_t)i * kM));
-      }
-    }
-  } else if (warp == 1 && lane == 0) {
-    // MMA issuer
-    if (ntiles > 0 && mbar_wait(qbar, 0)) {
-      const uint64_t bdesc = sdesc_sw128(sq);
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i % kStages;
-        const int a = i & 1;
-        if (i >= 2 && !mbar_wait(&acce[a], ((i >> 1) & 1) ^ 1)) break;
-        if (!mbar_wait(&full[st], (i / kStages) & 1)) break;
-        tc_fence_after();
-        const uint64_t adesc = sdesc_sw128(sk + st * kTileK);
-        const uint32_t d = tmem + (uint32_t)(a * kN);
-#pragma unroll
-        for (int kk = 0; kk < kDim / kKStep; ++kk) {
-          // advance both start addresses by kk * 32 bytes inside the swizzled rows
-          umma_f8(d, adesc + (uint64_t)((kk * kKStep) >> 4), bdesc + (uint64_t)((kk * kKStep) >> 4), kk > 0);
+  if (warp < kCtrlWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+    if (warp == 0 && lane == 0) {
+      if (ntiles > 0) {
+        // TMA producer
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tk) : "memory");
+        mbar_expect_tx(qbar, kTileQ);
+        tma_load_2d(&tq, qbar, sq, 0, t0 * kHeads);
+        for (int i = 0; i < ntiles; ++i) {
+          const int st = i % kStages;
+          if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) break;
+          mbar_expect_tx(&full[st], kTileK + (i == 0 ? kStarveBytes : 0u));
+          tma_load_2d(&tk, &full[st], sk + st * kTileK, 0, (int)(klo + (int64_t)i * kM));
         }
-        umma_commit(&empty[st]);
-        umma_commit(&accf[a]);
+      }
+    } else if (warp == 1 && lane == 0) {
+      // MMA issuer
+      if (ntiles > 0 && mbar_wait(qbar, 0)) {
+        const uint64_t bdesc = sdesc_sw128(sq);
+        for (int i = 0; i < ntiles; ++i) {
+          const int st = i % kStages;
+          const int a = i & 1;
+          if (i >= 2 && !mbar_wait(&acce[a], ((i >> 1) & 1) ^ 1)) break;
+          if (!mbar_wait(&full[st], (i / kStages) & 1)) break;
+          tc_fence_after();
+          const uint64_t adesc = sdesc_sw128(sk + st * kTileK);
+          const uint32_t d = tmem + (uint32_t)(a * kN);
+  #pragma unroll
+          for (int kk = 0; kk < kDim / kKStep; ++kk) {
+            // advance both start addresses by kk * 32 bytes inside the swizzled rows
+            umma_f8(d, adesc + (uint64_t)((kk * kKStep) >> 4), bdesc + (uint64_t)((kk * kKStep) >> 4), kk > 0);
+          }
+          umma_commit(&empty[st]);
+          umma_commit(&accf[a]);
+        }
       }
     }
-  } else if (warp >= 2) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
     // epilogue: thread = key row m of the tile (TMEM lane); warp % 4 picks the
     // lane quarter, the four warps of a quarter group each own one query
     static_assert(kEpiWarps == 4 * kQueriesPerCta, "one query per epilogue warp");
     const int sub = warp & 3;
-    const int q = (warp - 2) >> 2;
+    const int q = (warp - kCtrlWarps) >> 2;
     const int m = sub * 32 + lane;
-    const int lt = ((warp - 2) & 3) * 32 + lane;  // thread index within the query's group
+    const int lt = ((warp - kCtrlWarps) & 3) * 32 + lane;  // thread index within the query's group
     const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
-    const float4* w4 = reinterpret_cast<const float4*>(ws);
+    // this warp's query's 64 head weights, held in registers for the whole loop
+    float4 wr[kHeads / 4];
+#pragma unroll
+    for (int j = 0; j < kHeads / 4; ++j) wr[j] = reinterpret_cast<const float4*>(ws)[q * (kHeads / 4) + j];
     // this warp's query's live span, read once
     int64_t qs0 = 0, qs1 = 0;
     if (q < nq) {
@@ -446,37 +479,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&accf[a], (i >> 1) & 1));
       if (ok) {
         tc_fence_after();
-        uint32_t r0[32], r1[32];
         const uint32_t col = lane_addr + (uint32_t)(a * kN + q * kHeads);
-        // heads 0-31 and 32-63; the fused form reads the second half after
-        // reducing the first, so both halves never hold registers together
-        tmem_ld32(col, r0);
-        if constexpr (!kFused) tmem_ld32(col + 32u, r1);
-        tmem_wait_ld();
-        // four independent partial sums (one per float4 lane) keep the FMA
-        // dependency chains short; the order of the sums is the same in both
-        // forms, so their values are bit-identical
-        float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        // 16 heads at a time; two packed partial sums (heads 0,1 and 2,3 mod
+        // 4) keep the FMA chains short.  The order of the sums is fixed, so
+        // both forms produce bit-identical values.
+        uint64_t acc01 = 0ull, acc23 = 0ull;
+        uint32_t r[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 wv = w4[q * (kHeads / 4) + j];
-          acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r0[4 * j + 0]), 0.f), acc0);
-          acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r0[4 * j + 1]), 0.f), acc1);
-          acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r0[4 * j + 2]), 0.f), acc2);
-          acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r0[4 * j + 3]), 0.f), acc3);
-        }
-        if constexpr (kFused) {
-          tmem_ld32(col + 32u, r1);
+        for (int c = 0; c < kHeads / 16; ++c) {
+          tmem_ld16(col + 16u * c, r);
           tmem_wait_ld();
-        }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const float4 wv = w4[q * (kHeads / 4) + 8 + j];
-          acc0 = fmaf(wv.x, fmaxf(__uint_as_float(r1[4 * j + 0]), 0.f), acc0);
-          acc1 = fmaf(wv.y, fmaxf(__uint_as_float(r1[4 * j + 1]), 0.f), acc1);
-          acc2 = fmaf(wv.z, fmaxf(__uint_as_float(r1[4 * j + 2]), 0.f), acc2);
-          acc3 = fmaf(wv.w, fmaxf(__uint_as_float(r1[4 * j + 3]), 0.f), acc3);
+          for (int j = 0; j < 4; ++j) {
+            const float4 wv = wr[4 * c + j];
+            acc01 = ffma2(pack2(wv.x, wv.y),
+                          pack2(fmaxf(__uint_as_float(r[4 * j + 0]), 0.f), fmaxf(__uint_as_float(r[4 * j + 1]), 0.f)),
+                          acc01);
+            acc23 = ffma2(pack2(wv.z, wv.w),
+                          pack2(fmaxf(__uint_as_float(r[4 * j + 2]), 0.f), fmaxf(__uint_as_float(r[4 * j + 3]), 0.f)),
+                          acc23);
+          }
         }
+        float acc0, acc1, acc2, acc3;
+        unpack2(acc01, acc0, acc1);
+        unpack2(acc23, acc2, acc3);
         const float v = ((acc0 + acc1) + (acc2 + acc3)) * ksc;
         if constexpr (!kFused) {
           if (s >= qs0 && s < qs1) p.out[(int64_t)(t0 + q) * p.ld + s] = v;
