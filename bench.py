@@ -400,6 +400,7 @@ def measure_extras(dsa, torch, dev, local, prefill):
     out["combine_window_prefill_1m"] = {"window": window, "us_per_launch": us,
                                         "achieved_gbs": comb_alg / (us * 1e-6) / 1e9}
     out["indexer_producer"] = measure_producer(dsa, torch, dev)
+    out["indexer_select_fused"] = measure_fused(dsa, torch, dev)
     return out
 
 
@@ -435,6 +436,49 @@ def measure_producer(dsa, torch, dev, T=608, S=131072):
     tf = flops / (ms / 1e3) / 1e12
     return {"queries": T, "keys": S, "ms_per_launch": ms, "tflops": tf, "peak_tflops": peak,
             "frac": tf / peak, "peak_source": src, "status": dsa.dsa_indexer_status()}
+
+
+def measure_fused(dsa, torch, dev, T=608, S=131072, B=8, Kb=256, K=2048):
+    """The producer fused with the selection (dsa_indexer_select) against the
+    two-step path (dsa_indexer_logits, then dsa_select_topk) on the same causal
+    queries; both give the same cand / topk."""
+    q, k, ks, w, _, ends = wk.indexer_inputs(T, S, seed=11)
+    qd, kd = torch.from_numpy(q).to(dev), torch.from_numpy(k).to(dev)
+    ksd, wd = torch.from_numpy(ks).to(dev), torch.from_numpy(w).to(dev)
+    en = torch.from_numpy(ends).to(dev)
+    plan = dsa.dsa_select_init(rows=T, width=S, block_size=B, block_topk=Kb, row_topk=K)
+    logits = torch.empty((T, S), dtype=torch.float32, device=dev)
+    cand2 = torch.empty((T, Kb + 1), dtype=torch.int32, device=dev)
+    topk2 = torch.empty((T, K), dtype=torch.int32, device=dev)
+    ws_bytes = dsa.dsa_indexer_select_workspace(plan)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    cand = torch.empty((T, Kb + 1), dtype=torch.int32, device=dev)
+    topk = torch.empty((T, K), dtype=torch.int32, device=dev)
+
+    def two_step():
+        dsa.dsa_indexer_logits(qd, kd, ksd, wd, None, en, logits)
+        dsa.dsa_select_topk(plan, logits, None, en, cand2, topk2)
+
+    def fused():
+        dsa.dsa_indexer_select(plan, qd, kd, ksd, wd, en, ws, cand, topk)
+
+    res = {"queries": T, "keys": S, "block_size": B, "block_topk": Kb, "row_topk": K}
+    for name, fn in (("two_step", two_step), ("fused", fused)):
+        for _ in range(3):
+            fn()
+        e0, e1 = _events(torch, 2)
+        e0.record()
+        for _ in range(10):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / 10
+        res[name] = {"us_per_call": us, "rows_per_s": T / (us * 1e-6)}
+    res["fused_workspace_bytes"] = int(ws_bytes)
+    res["two_step_logits_bytes"] = int(T * S * 4)
+    res["same_result"] = bool(torch.equal(cand, cand2) and torch.equal(topk, topk2))
+    res["status"] = dsa.dsa_indexer_status()
+    return res
 
 
 # ---------------------------------------------------------------------------
@@ -578,6 +622,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--producer-only", nargs=2, type=int, metavar=("QUERIES", "KEYS"),
                     help="time only the tensor-core indexer-logits producer and print its JSON")
+    ap.add_argument("--fused-only", nargs=2, type=int, metavar=("QUERIES", "KEYS"),
+                    help="time only the fused producer + selection against the two-step path")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the supplementary decode / single-row / scan-mode timings")
     ap.add_argument("--rows", type=int, default=None,
@@ -587,15 +633,15 @@ def main():
     args = ap.parse_args()
     if args.warmup < 1:
         ap.error("--warmup must be >= 1")
-    if args.producer_only:
+    if args.producer_only or args.fused_only:
         import torch
 
         import sparse_attention_indexer_live_gb300 as dsa
         dsa.build()
         dsa.load()
-        T, S = args.producer_only
-        print(json.dumps(measure_producer(dsa, torch, torch.device("cuda:0"), T=T, S=S)),
-              flush=True)
+        fn, (T, S) = ((measure_producer, args.producer_only) if args.producer_only
+                      else (measure_fused, args.fused_only))
+        print(json.dumps(fn(dsa, torch, torch.device("cuda:0"), T=T, S=S)), flush=True)
         return
     wl = wk.WORKLOADS[args.workload]
     if args.rows is not None:

@@ -21,15 +21,16 @@
 //               row's 64 columns of one query with tcgen05.ld, weighted ReLU sum
 //               over the heads (weights in registers, packed FMAs), coalesced
 //               fp32 stores of the live span
-// Fused form (dsa_indexer_select): the same epilogue values, never stored.
-// Each query's four warps reduce them to block maxima (shuffles across B
-// lanes) and keep a streaming top-Kb of blocks in shared memory: a slot per
-// block that beats the running threshold, its B values beside it, plus a copy
-// of the last live block's values.  One reducing barrier per tile decides, for
-// the four warps together, whether the 512-slot buffer must be compacted
-// (bitonic sort of a copy, keep the Kb best, rebuild the free-slot stack).  At
-// the end each query's buffer becomes a workspace record, from which the
-// selection side finishes the block top-k and takes the row top-k.
+// Fused form (dsa_indexer_select): the same epilogue values, never stored as
+// a logits matrix.  Each query's four warps keep a streaming top-Kb of block
+// maxima: one warp vote per tile against the threshold's key settles most
+// tiles; otherwise block maxima (shuffles across B lanes) that beat the
+// threshold take a shared-memory slot, and their B values go to that slot of
+// the query's workspace record, as do the last live block's values.  Every few
+// tiles one reducing barrier decides, for the four warps together, whether the
+// 2048-slot buffer must be compacted (radix select of the Kb-th best, free the
+// rest, rebuild the free-slot stack).  At the end the slots go to the record,
+// from which the selection side finishes the block top-k and the row top-k.
 // Every mbarrier wait is bounded by a clock limit; a wait that runs out sets a
 // device error word (read by dsa_indexer_status) and the CTA winds down.
 
@@ -108,6 +109,7 @@ struct IdxParams {
   int32_t B;       // block size, a power of two <= 8
   int32_t log2B;
   int32_t Kb;      // <= kFusedMaxKb
+  int32_t check_tiles;  // tiles between capacity checks, a power of two
 };
 
 
@@ -231,19 +233,26 @@ constexpr int kOffW = (kOffTmem + 4 + 15) & ~15;
 constexpr int kSmemUsed = kOffW + kQueriesPerCta * kHeads * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024-byte alignment
 
-// Per-query streaming state of the fused variant:
-//   comp[cap] u64 (0 = free slot) | temp[cap] u64 (compaction scratch) |
-//   vals[cap * 8] f32 (the slot's block values) | freeq[cap] u16 (free slots) |
-//   last[8] f32 (the last live block's values) | insertion counter i32 | tau u64 | scan[4] i32
+// Per-query streaming state of the fused variant (the slots' values live in
+// the workspace record, written when a slot is filled):
+//   comp[cap] u64 (0 = free slot) | freeq[cap] u16 (free slots, in slot order) |
+//   hist[256] u32 (compaction scratch) | insertion counter i32 | sel[3] u32 |
+//   tau u64 | scan[4] i32
 constexpr int kQsComp = 0;
-constexpr int kQsTemp = kQsComp + kFusedCap * 8;
-constexpr int kQsVals = kQsTemp + kFusedCap * 8;
-constexpr int kQsFree = kQsVals + kFusedCap * kFusedMaxB * 4;
-constexpr int kQsLast = kQsFree + kFusedCap * 2;
-constexpr int kQsCnt = kQsLast + kFusedMaxB * 4;
-constexpr int kQsTau = kQsCnt + 8;
+constexpr int kQsFree = kQsComp + kFusedCap * 8;
+constexpr int kQsHist = kQsFree + kFusedCap * 2;
+constexpr int kQsCnt = kQsHist + 256 * 4;
+constexpr int kQsSel = kQsCnt + 4;
+constexpr int kQsTau = kQsSel + 12;
 constexpr int kQsScan = kQsTau + 8;
 constexpr int kQsBytes = (kQsScan + 16 + 127) & ~127;
+// Capacity checks every E tiles (E = IdxParams::check_tiles, a power of two):
+// a tile inserts at most 128 / B blocks per query, so a buffer at or below
+// cap - E * 128 / B entries takes the next E tiles without a check.  The host
+// picks the largest E <= 16 that leaves room for two such intervals after a
+// compaction to Kb entries.
+constexpr int kMaxCheckTiles = 16;
+static_assert(kFusedCap - 2 * kM >= kFusedMaxKb, "the buffer must keep room after a compaction");
 constexpr int kOffQs = (kSmemUsed + 127) & ~127;
 constexpr int kSmemFused = kOffQs + kQueriesPerCta * kQsBytes + 1024;
 
@@ -272,43 +281,93 @@ __device__ __forceinline__ bool group_any(int q, bool v) {
   return r != 0;
 }
 
-// Keep the Kb best entries of a query's buffer: an ascending bitonic sort of a
-// copy gives the Kb-th best X; entries below X are freed in place (values stay
-// in their slots) and the free-slot stack is rebuilt in slot order.  Called by
-// the query's 128 epilogue threads (lt = 0..127).
+// The k-th largest of a query's n composites (zero = free slot; k <= the
+// number of non-zero entries), by an MSB-first radix select on 8-bit digits
+// over the query's 128 epilogue threads: a shared histogram per digit (lanes
+// with equal digits add once), one warp locates the digit holding the k-th,
+// and the select stops as soon as that digit's bucket is exactly what is left.
+__device__ uint64_t group_kth(const uint64_t* a, int n, int k, uint32_t* hist, uint32_t* sel, int q, int lt) {
+  const int lane = lt & 31;
+  uint64_t prefix = 0, mask = 0;
+  uint32_t kk = (uint32_t)k;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = lt; i < 256; i += 128) hist[i] = 0;
+    group_bar(q);
+    for (int i0 = 0; i0 < n; i0 += 128) {
+      const int i = i0 + lt;
+      bool in = false;
+      uint32_t d = 0;
+      if (i < n) {
+        const uint64_t v = a[i];
+        in = (v & mask) == prefix;
+        d = (uint32_t)(v >> shift) & 0xFFu;
+      }
+      const uint32_t act = __ballot_sync(0xFFFFFFFFu, in);
+      if (in) {
+        const uint32_t peers = __match_any_sync(act, d);
+        if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
+      }
+    }
+    group_bar(q);
+    if (lt < 32) {
+      uint32_t h[8];
+      uint32_t tot = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        h[j] = hist[8 * lane + j];
+        tot += h[j];
+      }
+      uint32_t incl = tot;  // entries in this lane's bins and above
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
+        if (lane + o < 32) incl += y;
+      }
+      uint32_t cum = incl - tot;  // entries in higher bins
+#pragma unroll
+      for (int j = 7; j >= 0; --j) {
+        if (cum < kk && cum + h[j] >= kk) {
+          sel[0] = (uint32_t)(8 * lane + j);
+          sel[1] = cum;
+          sel[2] = h[j];
+        }
+        cum += h[j];
+      }
+    }
+    group_bar(q);
+    const uint32_t d = sel[0], above = sel[1], cnt = sel[2];
+    kk -= above;
+    prefix |= (uint64_t)d << shift;
+    mask |= (uint64_t)0xFFu << shift;
+    if (cnt == kk) break;
+  }
+  // every thread has read sel before the next call writes it
+  group_bar(q);
+  return prefix;
+}
+
+// Keep the Kb best entries of a query's buffer: X = the Kb-th best; entries
+// below X are freed in place (values stay in their record slots) and the
+// free-slot stack is rebuilt in slot order.  Called by the query's 128
+// epilogue threads (lt = 0..127) when the buffer holds more than Kb entries.
 __device__ __noinline__ void fused_compact(uint8_t* qs, int q, int lt, int Kb) {
   uint64_t* comp = reinterpret_cast<uint64_t*>(qs + kQsComp);
-  uint64_t* temp = reinterpret_cast<uint64_t*>(qs + kQsTemp);
   uint16_t* freeq = reinterpret_cast<uint16_t*>(qs + kQsFree);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(qs + kQsHist);
+  uint32_t* sel = reinterpret_cast<uint32_t*>(qs + kQsSel);
   int* cnt = reinterpret_cast<int*>(qs + kQsCnt);
   uint64_t* tau = reinterpret_cast<uint64_t*>(qs + kQsTau);
   int* scan = reinterpret_cast<int*>(qs + kQsScan);
-  for (int i = lt; i < kFusedCap; i += 128) temp[i] = comp[i];
-  group_bar(q);
-  for (int k = 2; k <= kFusedCap; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = lt; i < kFusedCap; i += 128) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t x = temp[i], y = temp[ixj];
-          if ((x > y) == ((i & k) == 0)) {
-            temp[i] = y;
-            temp[ixj] = x;
-          }
-        }
-      }
-      group_bar(q);
-    }
-  }
-  const uint64_t X = temp[kFusedCap - Kb];  // the Kb-th largest
-  for (int i = lt; i < kFusedCap; i += 128)
-    if (comp[i] < X) comp[i] = 0;
-  group_bar(q);
-  // free slots, ascending: 4 consecutive slots per thread, prefix over 128 threads
+  const uint64_t X = group_kth(comp, kFusedCap, Kb, hist, sel, q, lt);
+  // free slots, ascending: kPer consecutive slots per thread, prefix over 128 threads
   constexpr int kPer = kFusedCap / 128;
   int c = 0;
 #pragma unroll
-  for (int i = 0; i < kPer; ++i) c += comp[kPer * lt + i] == 0;
+  for (int i = 0; i < kPer; ++i) {
+    uint64_t& e = comp[kPer * lt + i];
+    if (e < X) e = 0;
+    c += e == 0;
+  }
   const int lane = lt & 31, wq = lt >> 5;
   int incl = c;
 #pragma unroll
@@ -466,9 +525,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     uint8_t* qst = base + kOffQs + q * kQsBytes;
     const int nbq = (kFused && qs1 > 0) ? (int)((qs1 + p.B - 1) >> p.log2B) : 0;
-    uint64_t tau = 0;
-    int valid = 0;   // entries kept by the last compaction (0 or Kb)
-    int used = 0;    // this warp's latest view of the insertions since then
+    // the tile holding the query's last live block (start 0: klo is 0)
+    const int i_last = nbq > 0 ? (int)(((int64_t)(nbq - 1) << p.log2B) / kM) : -1;
+    // this query's record (only dereferenced for real queries, q < nq)
+    float* rec_vals = reinterpret_cast<float*>(p.ws + (int64_t)(t0 + q) * p.ws_stride + (int64_t)kFusedCap * 8);
+    float* rec_last = rec_vals + (int64_t)kFusedCap * p.B;
+    uint64_t tau = 0;     // insertion threshold: the Kb-th best at the last compaction
+    uint32_t tau_key = 0; // its order key: a block can beat tau only with a key at least this
+    int valid = 0;        // entries kept by the last compaction (0 or Kb)
+    int used = 0;         // this warp's latest view of the insertions since then
     int64_t s = klo + m;
     float ksc = s < khi ? p.k_scale[s] : 0.f;
     for (int i = 0; i < ntiles; ++i, s += kM) {
@@ -507,52 +572,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (!kFused) {
           if (s >= qs0 && s < qs1) p.out[(int64_t)(t0 + q) * p.ld + s] = v;
         } else {
-          // block maxima over B consecutive keys (lanes), then the query's
-          // streaming top-Kb: a slot per winning block, its B values beside it
+          // The query's streaming top-Kb of block maxima.  Most tiles are
+          // settled by one vote: no key of the warp reaches tau's key, so no
+          // block of the warp can enter the buffer.
           const int Bq = p.B;
-          uint32_t mx = s < qs1 ? okey(__float_as_uint(v)) : 0u;
-          for (int o = 1; o < Bq; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-          const int jb = (int)(s >> p.log2B);
-          const uint64_t c = ocomp(mx, (uint32_t)jb);
-          const bool ins = ((lane & (Bq - 1)) == 0) && jb < nbq && c > tau;
-          const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ins);
-          if (bal) {
-            int* cnt = reinterpret_cast<int*>(qst + kQsCnt);
-            const int leader = __ffs(bal) - 1;
-            int basei = 0;
-            if (lane == leader) basei = atomicAdd(&cnt[0], __popc(bal));
-            basei = __shfl_sync(0xFFFFFFFFu, basei, leader);
-            used = basei + __popc(bal);
-            int slot = -1;
-            if (ins) {
-              const int idx = basei + __popc(bal & lanemask_lt_u());
-              if (idx < kFusedCap - valid) {
-                slot = reinterpret_cast<const uint16_t*>(qst + kQsFree)[idx];
-                reinterpret_cast<uint64_t*>(qst + kQsComp)[slot] = c;
-              } else {
-                atomicExch(&g_indexer_error, 2);  // unreachable: the capacity check keeps a tile's room
+          const uint32_t key = okey(__float_as_uint(v));
+          const bool live = s < qs1;
+          if (__ballot_sync(0xFFFFFFFFu, live && key >= tau_key)) {
+            // block maxima over B consecutive keys (lanes)
+            uint32_t mx = live ? key : 0u;
+            for (int o = 1; o < Bq; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+            const int jb = (int)(s >> p.log2B);
+            const uint64_t c = ocomp(mx, (uint32_t)jb);
+            const bool ins = ((lane & (Bq - 1)) == 0) && live && c > tau;
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ins);
+            if (bal) {
+              int* cnt = reinterpret_cast<int*>(qst + kQsCnt);
+              const int leader = __ffs(bal) - 1;
+              int basei = 0;
+              if (lane == leader) basei = atomicAdd(&cnt[0], __popc(bal));
+              basei = __shfl_sync(0xFFFFFFFFu, basei, leader);
+              used = basei + __popc(bal);
+              int slot = -1;
+              if (ins) {
+                const int idx = basei + __popc(bal & lanemask_lt_u());
+                if (idx < kFusedCap - valid) {
+                  slot = reinterpret_cast<const uint16_t*>(qst + kQsFree)[idx];
+                  reinterpret_cast<uint64_t*>(qst + kQsComp)[slot] = c;
+                } else {
+                  atomicExch(&g_indexer_error, 2);  // unreachable: the capacity checks keep room
+                }
               }
+              // the block's B values go to its slot of the record
+              const int bslot = __shfl_sync(0xFFFFFFFFu, slot, lane & ~(Bq - 1));
+              if (bslot >= 0) rec_vals[(int64_t)bslot * Bq + (lane & (Bq - 1))] = v;
             }
-            const int bslot = __shfl_sync(0xFFFFFFFFu, slot, lane & ~(Bq - 1));
-            if (bslot >= 0) reinterpret_cast<float*>(qst + kQsVals)[bslot * Bq + (lane & (Bq - 1))] = v;
           }
-          if (jb == nbq - 1) reinterpret_cast<float*>(qst + kQsLast)[lane & (Bq - 1)] = v;
+          // the last live block's values, kept whether or not it enters
+          if (i == i_last && (int)(s >> p.log2B) == nbq - 1) rec_last[lane & (Bq - 1)] = v;
         }
       }
       tc_fence_before();
       mbar_arrive(&acce[a]);
       ksc = ksc_next;
       if constexpr (kFused) {
-        // Capacity check, one reducing barrier per tile.  The shared counter
-        // is only ever raised by atomics, so the warp whose atomic came last
-        // saw the full count and the OR over the group is exact: all four
-        // warps take the same branch.
-        // A tile inserts at most 128 / B blocks per query; compacting once
-        // the buffer could not take another tile keeps every insertion in
-        // bounds.
-        if (i + 1 < ntiles && group_any(q, valid + used > kFusedCap - (kM >> p.log2B))) {
+        // Capacity check every check_tiles tiles, one reducing barrier.  The
+        // shared counter is only ever raised by atomics, so the warp whose
+        // atomic came last saw the full count and the OR over the group is
+        // exact: all four warps take the same branch.
+        if (((i + 1) & (p.check_tiles - 1)) == 0 && i + 1 < ntiles &&
+            group_any(q, valid + used > kFusedCap - p.check_tiles * (kM >> p.log2B))) {
           fused_compact(qst, q, lt, p.Kb);
           tau = *reinterpret_cast<const uint64_t*>(qst + kQsTau);
+          tau_key = (uint32_t)(tau >> 32);
           valid = p.Kb;
           used = 0;
         }
@@ -562,16 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the query's record for the finishing kernel
       group_bar(q);
       if (q < nq) {
-        uint8_t* rec = p.ws + (int64_t)(t0 + q) * p.ws_stride;
+        uint64_t* rc = reinterpret_cast<uint64_t*>(p.ws + (int64_t)(t0 + q) * p.ws_stride);
         const uint64_t* comp = reinterpret_cast<const uint64_t*>(qst + kQsComp);
-        const float* vals = reinterpret_cast<const float*>(qst + kQsVals);
-        uint64_t* rc = reinterpret_cast<uint64_t*>(rec);
-        float* rv = reinterpret_cast<float*>(rec + (int64_t)kFusedCap * 8);
-        float* rl = rv + (int64_t)kFusedCap * p.B;
-        const bool empty_row = ntiles == 0 || nbq == 0;
-        for (int i = lt; i < kFusedCap; i += 128) rc[i] = empty_row ? 0ull : comp[i];
-        for (int i = lt; i < kFusedCap * p.B; i += 128) rv[i] = vals[i];
-        if (lt < p.B) rl[lt] = reinterpret_cast<const float*>(qst + kQsLast)[lt];
+        for (int i = lt; i < kFusedCap; i += 128) rc[i] = comp[i];
       }
     }
   }
@@ -715,6 +780,8 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
   P.B = B;
   P.log2B = B == 1 ? 0 : B == 2 ? 1 : B == 4 ? 2 : 3;
   P.Kb = Kb;
+  P.check_tiles = kMaxCheckTiles;
+  while (P.check_tiles > 1 && 2 * P.check_tiles * (kM / B) > kFusedCap - kFusedMaxKb) P.check_tiles >>= 1;
   st = launch<true>(cfg, q, k, P, (cudaStream_t)stream);
   if (st != DSA_OK) return st;
   return dsa_fused_finish(plan, static_cast<const uint8_t*>(workspace), rec, ends, cand, topk,

@@ -15,15 +15,19 @@
 
 #define DSA_HIDDEN __attribute__((visibility("hidden")))
 
-// Streaming-buffer slots per query, kept in the record.
-constexpr int kFusedCap = 512;
+// Streaming-buffer slots per query, kept in the record.  With Kb <= 256 the
+// buffer holds well over a thousand insertions between two compactions, so a
+// query compacts only a few times whatever its length.
+constexpr int kFusedCap = 2048;
 constexpr int kFusedMaxB = 8;
 constexpr int kFusedMaxKb = 256;
 
 // One query's record: comp[kFusedCap] u64 (0 = empty slot; else the block's
 // (order key << 32) | (~block id)) | vals[kFusedCap * B] f32 (slot i holds its
 // block's B values at i * B) | last[B] f32 (the values of the query's last
-// live block, whether or not it was kept), padded to 16 bytes.
+// live block, whether or not it was kept), padded to 16 bytes.  The producer
+// writes a slot's values when the slot is filled and the comp array at the
+// end; only slots with a non-zero comp are meaningful.
 __host__ __device__ constexpr int64_t fused_record_bytes(int B) {
   return ((int64_t)kFusedCap * 8 + (int64_t)kFusedCap * B * 4 + (int64_t)B * 4 + 15) & ~(int64_t)15;
 }
