@@ -237,6 +237,38 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
                        void* workspace, size_t workspace_bytes, int32_t* cand, int32_t* topk,
                        struct CUstream_st* stream);
 
+/*
+ * dsa_indexer_select without a caller workspace: the fused producer +
+ * selection, with its per-query records kept in one fixed array inside this
+ * library instead of memory the caller allocates.  The pages describe nothing
+ * like it; it exists for callers of this library that cannot allocate device
+ * memory when they call: an engine that hands all free device memory to its
+ * own pool before serving (a cudaMalloc then fails, or bypasses the pool and
+ * fragments it), a plugin whose host framework owns the device allocator and
+ * allows no side allocations, or plain C code with no allocator to take a
+ * workspace from.  This call allocates nothing: no cudaMalloc, no cudaFree,
+ * no allocating library routine.
+ *   Limit: the array holds DSA_NOALLOC_SCRATCH_BYTES (8 MiB) on every device
+ *   that loads the library, until the process exits.  A plan whose
+ *   dsa_indexer_select_workspace() exceeds it gets DSA_ERR_UNSUPPORTED (about
+ *   100 queries at block size 8; 80 KB per query).
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture begins.
+ *   Sharing: every call on a device uses the same array, and each call
+ *   overwrites what the last one left there (nothing in it has to start at
+ *   zero: a call writes every part of it that it reads back).  Calls that can
+ *   run at the same time on the GPU -- on streams with no ordering between
+ *   them -- race on it; keep them on one stream or otherwise ordered.
+ * Arguments, results and errors are those of dsa_indexer_select.
+ */
+#define DSA_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+int dsa_indexer_select_noalloc(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg,
+                               const uint8_t* q, const uint8_t* k, const float* k_scale,
+                               const float* w, const int32_t* ends, int32_t* cand, int32_t* topk,
+                               struct CUstream_st* stream);
+
 /* Static description of a status code. */
 const char* dsa_status_string(int status);
 

@@ -5,9 +5,11 @@ The work runs in hand-written sm_103a CUDA kernels behind a C ABI
 Python binding over it.
 """
 from .binding import (DSA_ERR_CUDA, DSA_ERR_INVALID_ARG, DSA_ERR_TIMEOUT, DSA_ERR_UNSUPPORTED,
-                      DSA_OK, DsaSelectError, EXPORTS, Plan, dsa_candidate_select,
+                      DSA_OK, NOALLOC_SCRATCH_BYTES, DsaSelectError, EXPORTS, Plan,
+                      dsa_candidate_select,
                       dsa_combine_window, dsa_indexer_cfg, dsa_indexer_logits,
-                      dsa_indexer_select, dsa_indexer_select_workspace, dsa_indexer_status,
+                      dsa_indexer_select, dsa_indexer_select_noalloc,
+                      dsa_indexer_select_workspace, dsa_indexer_status,
                       dsa_plan_desc, dsa_row_topk, dsa_select_cfg, dsa_select_init,
                       dsa_select_topk, load, make_cfg, status_string)
 from .build import LIB_PATH, build
@@ -18,5 +20,6 @@ __all__ = ["DSA_OK", "DSA_ERR_INVALID_ARG", "DSA_ERR_UNSUPPORTED", "DSA_ERR_CUDA
            "dsa_plan_desc", "make_cfg", "dsa_select_init", "dsa_candidate_select",
            "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_indexer_cfg",
            "dsa_indexer_logits", "dsa_indexer_select", "dsa_indexer_select_workspace",
+           "dsa_indexer_select_noalloc", "NOALLOC_SCRATCH_BYTES",
            "dsa_indexer_status", "status_string", "load", "build", "LIB_PATH",
            "Shard", "ShardedSelector", "shard_rows"]

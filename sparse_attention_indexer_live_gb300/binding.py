@@ -38,7 +38,11 @@ class dsa_plan_desc(ctypes.Structure):
 EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_candidate_select",
            "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_indexer_logits",
            "dsa_indexer_status", "dsa_indexer_select_workspace", "dsa_indexer_select",
-           "dsa_status_string")
+           "dsa_indexer_select_noalloc", "dsa_status_string")
+
+# Size of the library's fixed scratch array used by dsa_indexer_select_noalloc
+# (DSA_NOALLOC_SCRATCH_BYTES in include/dsa_select.h).
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class dsa_indexer_cfg(ctypes.Structure):
@@ -91,6 +95,9 @@ def load(path: str | None = None):
             L.dsa_indexer_select.restype = i32
             L.dsa_indexer_select.argtypes = [vp, ctypes.POINTER(dsa_indexer_cfg), vp, vp, vp, vp,
                                              vp, vp, ctypes.c_size_t, vp, vp, vp]
+            L.dsa_indexer_select_noalloc.restype = i32
+            L.dsa_indexer_select_noalloc.argtypes = [vp, ctypes.POINTER(dsa_indexer_cfg), vp, vp, vp,
+                                                     vp, vp, vp, vp, vp]
             L.dsa_status_string.restype = ctypes.c_char_p
             L.dsa_status_string.argtypes = [i32]
             _lib = L
@@ -285,6 +292,32 @@ def dsa_indexer_select(plan: Plan, q, k, k_scale, w, ends, workspace, cand, topk
                                      _ptr(w), _ptr(ends), _ptr(workspace), workspace.numel(),
                                      _ptr(cand), _ptr(topk), _stream(stream)),
            "dsa_indexer_select")
+
+
+def dsa_indexer_select_noalloc(plan: Plan, q, k, k_scale, w, ends, cand, topk, stream=None):
+    """dsa_indexer_select for callers that cannot allocate device memory at
+    call time (an engine whose pool already owns the free memory, a plugin
+    under a host framework's allocator, C code with no allocator): the
+    per-query records go to a fixed 8 MiB array inside the library, so no
+    workspace is passed and nothing is allocated.  Batches whose workspace
+    (dsa_indexer_select_workspace) exceeds that array are refused.  All calls
+    on a device share the array: keep them ordered (one stream), and make the
+    first call on a device before any stream capture."""
+    import torch
+    T, H, D = q.shape
+    S = k.shape[0]
+    for name, t, dt in (("q", q, torch.uint8), ("k", k, torch.uint8), ("k_scale", k_scale,
+                        torch.float32), ("w", w, torch.float32), ("ends", ends, torch.int32)):
+        assert t.dtype == dt and t.is_cuda and t.is_contiguous(), name
+    c = plan.cfg
+    for name, t, cols in (("cand", cand, c.block_topk + 1), ("topk", topk, c.row_topk)):
+        assert t.dtype == torch.int32 and t.is_cuda and t.is_contiguous() and \
+            t.numel() >= c.rows * cols, f"{name}: CUDA int32 [rows, {cols}]"
+    cfg = dsa_indexer_cfg(queries=T, keys=S, heads=H, head_dim=D, out_stride=S)
+    _check(load().dsa_indexer_select_noalloc(plan.handle, ctypes.byref(cfg), _ptr(q), _ptr(k),
+                                             _ptr(k_scale), _ptr(w), _ptr(ends), _ptr(cand),
+                                             _ptr(topk), _stream(stream)),
+           f"dsa_indexer_select_noalloc (fixed scratch of {NOALLOC_SCRATCH_BYTES} bytes)")
 
 
 def dsa_indexer_status() -> int:

@@ -40,6 +40,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "dsa_internal.h"
 
 namespace {
@@ -786,6 +788,65 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
   if (st != DSA_OK) return st;
   return dsa_fused_finish(plan, static_cast<const uint8_t*>(workspace), rec, ends, cand, topk,
                           (cudaStream_t)stream);
+}
+
+}  // extern "C"
+
+// The allocation-free variant's records: one fixed array per device, in the
+// module, so the call never allocates.  Host code must not pass the array's
+// name to a kernel (on the host it is only a stand-in for the symbol); the
+// device address comes from cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kNoallocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kNoallocMaxDevices];
+
+// The array's device address on the current device; the first request on a
+// device looks it up with that device current.
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DSA_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kNoallocMaxDevices) return DSA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return DSA_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsa_indexer_select_noalloc(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, const uint8_t* q,
+                               const uint8_t* k, const float* k_scale, const float* w, const int32_t* ends,
+                               int32_t* cand, int32_t* topk, struct CUstream_st* stream) {
+  int32_t rows = 0, B = 0, Kb = 0;
+  int64_t width = 0;
+  const int st = dsa_fused_shape(plan, &rows, &width, &B, &Kb);
+  if (st != DSA_OK) return st;
+  // a batch whose records do not fit the fixed array is refused outright
+  if ((uint64_t)rows * (uint64_t)fused_record_bytes(B) > (uint64_t)DSA_NOALLOC_SCRATCH_BYTES)
+    return DSA_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  if (rows > 0) {
+    const int s2 = noalloc_scratch(&scratch);
+    if (s2 != DSA_OK) return s2;
+  }
+  return dsa_indexer_select(plan, cfg, q, k, k_scale, w, ends, scratch, DSA_NOALLOC_SCRATCH_BYTES, cand, topk,
+                            stream);
 }
 
 int dsa_indexer_status(void) {
