@@ -206,28 +206,28 @@ int dsa_indexer_status(void);
 /*
  * The producer fused with the selection, the [queries, keys] logits never
  * written.  Each query's logits are the ones dsa_indexer_logits computes
- * (start 0, live span [0, min(end_t, keys))); the launch reduces them to block
- * maxima and a streaming top-Kb per query while they are still in registers,
- * keeping every kept block's B values beside it, and leaves one record per
- * query in `workspace`.  A second launch finishes the block top-k (pin,
- * packed-column clamp, edge flag) and takes the row top-k exactly as
- * dsa_select_topk does on the materialised logits: cand and topk are
- * bit-identical to dsa_indexer_logits followed by dsa_select_topk.  No masked
- * logits are produced (there is no logits matrix).  The pages materialise the
- * score matrix (vLLM PR #48726, Motivation; vLLM PR #57459, Summary); the
- * fusion is this library's own.
+ * (start 0, live span [0, min(end_t, keys))).  Four launches share one record
+ * per query in `workspace`: the producer stores each live block's largest
+ * logit (4 bytes per block of B keys); the block top-k (pin, packed-column
+ * clamp, edge flag) runs on those maxima; the producer recomputes the logits
+ * of the kept blocks only, with the same tensor-core instruction and the same
+ * arithmetic, so they have the same bits; the row top-k runs on them.  cand
+ * and topk are bit-identical to dsa_indexer_logits followed by
+ * dsa_select_topk.  No masked logits are produced (there is no logits
+ * matrix).  The pages materialise the score matrix (vLLM PR #48726,
+ * Motivation; vLLM PR #57459, Summary); the fusion is this library's own.
  *   plan       from dsa_select_init with rows == queries, width == keys,
  *              col_stride 1, has_starts 0, row_repeat 1, block_size in
- *              {1, 2, 4, 8} and block_topk <= 256; any other plan gives
- *              DSA_ERR_UNSUPPORTED
+ *              {1, 2, 4, 8}; any other plan gives DSA_ERR_UNSUPPORTED
  *   cfg        queries == plan rows, keys == plan width, heads 64, head_dim 128
  *   q, k, k_scale, w, ends   as for dsa_indexer_logits (no starts)
  *   workspace  device memory, 16-byte aligned, of at least
- *              dsa_indexer_select_workspace() bytes; owned by the caller and
+ *              dsa_indexer_select_workspace() bytes (per query 4 * ceil(keys /
+ *              B) bytes plus about (Kb + 1) * (B + 1) * 4); owned by the caller and
  *              overwritten by every call, so calls that may overlap in time
  *              need workspaces of their own
  *   cand, topk int32 [queries, Kb + 1] and [queries, K], as dsa_select_topk
- * Returns DSA_OK once both launches are queued; bounded-wait timeouts are
+ * Returns DSA_OK once the launches are queued; bounded-wait timeouts are
  * reported by dsa_indexer_status() as for dsa_indexer_logits.
  */
 int dsa_indexer_select_workspace(const dsa_select_plan* plan, size_t* bytes);
@@ -250,8 +250,9 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
  * no allocating library routine.
  *   Limit: the array holds DSA_NOALLOC_SCRATCH_BYTES (8 MiB) on every device
  *   that loads the library, until the process exits.  A plan whose
- *   dsa_indexer_select_workspace() exceeds it gets DSA_ERR_UNSUPPORTED (about
- *   100 queries at block size 8; 80 KB per query).
+ *   dsa_indexer_select_workspace() exceeds it gets DSA_ERR_UNSUPPORTED (at
+ *   block size 8 and Kb 256: about 110 queries of 131,072 keys, 16 of
+ *   1,048,576).
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture begins.

@@ -21,16 +21,16 @@
 //               row's 64 columns of one query with tcgen05.ld, weighted ReLU sum
 //               over the heads (weights in registers, packed FMAs), coalesced
 //               fp32 stores of the live span
-// Fused form (dsa_indexer_select): the same epilogue values, never stored as
-// a logits matrix.  Each query's four warps keep a streaming top-Kb of block
-// maxima: one warp vote per tile against the threshold's key settles most
-// tiles; otherwise block maxima (shuffles across B lanes) that beat the
-// threshold take a shared-memory slot, and their B values go to that slot of
-// the query's workspace record, as do the last live block's values.  Every few
-// tiles one reducing barrier decides, for the four warps together, whether the
-// 2048-slot buffer must be compacted (radix select of the Kb-th best, free the
-// rest, rebuild the free-slot stack).  At the end the slots go to the record,
-// from which the selection side finishes the block top-k and the row top-k.
+// Fused form (dsa_indexer_select), four launches, no logits matrix:
+//   1. this kernel, block-max mode: the same epilogue values, reduced to each
+//      live block's largest logit (shuffles across B lanes) and stored in the
+//      query's workspace record -- 4 bytes per block instead of 4 per key;
+//   2. the selection side's block top-k over those maxima (cand, and the
+//      list of blocks whose logits the row top-k reads);
+//   3. this kernel, gather mode: the listed blocks' keys, loaded as 8-row TMA
+//      boxes, go through the same MMA instruction and the same epilogue
+//      routine, so each recomputed logit has the bits the first launch saw;
+//   4. the selection side's row top-k from those logits.
 // Every mbarrier wait is bounded by a clock limit; a wait that runs out sets a
 // device error word (read by dsa_indexer_status) and the CTA winds down.
 
@@ -104,14 +104,14 @@ struct IdxParams {
   int64_t ld;
   int32_t T;
   int32_t S;
-  // fused selection (kFused): per-query streaming block top-Kb state is dumped
-  // to ws + t * ws_stride bytes
+  // fused form: one record per query at ws + t * ws_stride (see dsa_internal.h)
   uint8_t* ws;
   int64_t ws_stride;
-  int32_t B;       // block size, a power of two <= 8
+  int64_t info_off;
+  int64_t vals_off;
+  int32_t B;       // block size, a power of two <= kFusedMaxB
   int32_t log2B;
-  int32_t Kb;      // <= kFusedMaxKb
-  int32_t check_tiles;  // tiles between capacity checks, a power of two
+  int32_t Kb;      // block top-k: a record lists at most Kb + 1 blocks
 };
 
 
@@ -226,7 +226,6 @@ __device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
 
 // Dynamic shared memory, from a 1024-aligned base:
 //   Q tile [256 x 128 B] | K ring [4 x 128 x 128 B] | mbarriers | TMEM address | w [4 x 64] f32
-//   | (fused only) per-query streaming state x 4
 constexpr int kOffK = kTileQ;
 constexpr int kOffBar = kOffK + kStages * kTileK;
 constexpr int kNumBars = 2 * kStages + 2 + 2 + 1;
@@ -235,163 +234,78 @@ constexpr int kOffW = (kOffTmem + 4 + 15) & ~15;
 constexpr int kSmemUsed = kOffW + kQueriesPerCta * kHeads * 4;
 constexpr int kSmemBytes = kSmemUsed + 1024;  // slack for the 1024-byte alignment
 
-// Per-query streaming state of the fused variant (the slots' values live in
-// the workspace record, written when a slot is filled):
-//   comp[cap] u64 (0 = free slot) | freeq[cap] u16 (free slots, in slot order) |
-//   hist[256] u32 (compaction scratch) | insertion counter i32 | sel[3] u32 |
-//   tau u64 | scan[4] i32
-constexpr int kQsComp = 0;
-constexpr int kQsFree = kQsComp + kFusedCap * 8;
-constexpr int kQsHist = kQsFree + kFusedCap * 2;
-constexpr int kQsCnt = kQsHist + 256 * 4;
-constexpr int kQsSel = kQsCnt + 4;
-constexpr int kQsTau = kQsSel + 12;
-constexpr int kQsScan = kQsTau + 8;
-constexpr int kQsBytes = (kQsScan + 16 + 127) & ~127;
-// Capacity checks every E tiles (E = IdxParams::check_tiles, a power of two):
-// a tile inserts at most 128 / B blocks per query, so a buffer at or below
-// cap - E * 128 / B entries takes the next E tiles without a check.  The host
-// picks the largest E <= 16 that leaves room for two such intervals after a
-// compaction to Kb entries.
-constexpr int kMaxCheckTiles = 16;
-static_assert(kFusedCap - 2 * kM >= kFusedMaxKb, "the buffer must keep room after a compaction");
-constexpr int kOffQs = (kSmemUsed + 127) & ~127;
-constexpr int kSmemFused = kOffQs + kQueriesPerCta * kQsBytes + 1024;
+// What a launch computes.
+constexpr int kModeLogits = 0;    // every live logit, stored in the [queries, out_stride] matrix
+constexpr int kModeBlockMax = 1;  // fused form: each live block's largest logit, into the record
+constexpr int kModeGather = 2;    // fused form: the logits of the record's listed blocks only
+// In the gather mode a K tile is 16 groups of 8 consecutive keys, one group per
+// listed block (the 8-key group holding it; B <= 8 divides 8) plus one for the
+// edge column; each group is its own 8-row TMA box, which lands in shared
+// memory exactly as 8 rows of a 128-row box would (one 1024-byte swizzle atom).
+constexpr int kGroupRows = 8;
+constexpr int kGroupsPerTile = kM / kGroupRows;
 
 __device__ __forceinline__ uint32_t okey(uint32_t u) { return u ^ ((uint32_t)((int32_t)u >> 31) | 0x80000000u); }
-__device__ __forceinline__ uint64_t ocomp(uint32_t key, uint32_t idx) {
-  return ((uint64_t)key << 32) | (uint64_t)(0xFFFFFFFFu - idx);
-}
-__device__ __forceinline__ uint32_t lanemask_lt_u() {
-  uint32_t m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-// Barrier of one query's four epilogue warps (ids 1..4; 0 is __syncthreads).
-__device__ __forceinline__ void group_bar(int q) {
-  asm volatile("bar.sync %0, %1;" ::"r"(1 + q), "r"(128) : "memory");
-}
-// The same barrier, returning whether any of the 128 threads passed true.
-__device__ __forceinline__ bool group_any(int q, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n"
-      " bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(1 + q), "r"(128)
-      : "memory");
-  return r != 0;
-}
+// The fp32 bits whose order key is k.
+__device__ __forceinline__ uint32_t okey_inv(uint32_t k) { return (k & 0x80000000u) ? (k ^ 0x80000000u) : ~k; }
 
-// The k-th largest of a query's n composites (zero = free slot; k <= the
-// number of non-zero entries), by an MSB-first radix select on 8-bit digits
-// over the query's 128 epilogue threads: a shared histogram per digit (lanes
-// with equal digits add once), one warp locates the digit holding the k-th,
-// and the select stops as soon as that digit's bucket is exactly what is left.
-__device__ uint64_t group_kth(const uint64_t* a, int n, int k, uint32_t* hist, uint32_t* sel, int q, int lt) {
-  const int lane = lt & 31;
-  uint64_t prefix = 0, mask = 0;
-  uint32_t kk = (uint32_t)k;
-  for (int shift = 56; shift >= 0; shift -= 8) {
-    for (int i = lt; i < 256; i += 128) hist[i] = 0;
-    group_bar(q);
-    for (int i0 = 0; i0 < n; i0 += 128) {
-      const int i = i0 + lt;
-      bool in = false;
-      uint32_t d = 0;
-      if (i < n) {
-        const uint64_t v = a[i];
-        in = (v & mask) == prefix;
-        d = (uint32_t)(v >> shift) & 0xFFu;
-      }
-      const uint32_t act = __ballot_sync(0xFFFFFFFFu, in);
-      if (in) {
-        const uint32_t peers = __match_any_sync(act, d);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[d], (uint32_t)__popc(peers));
-      }
+// One logit from this thread's TMEM lane: the query's 64 head scores in
+// 16-column chunks, weighted ReLU sum with two packed partial sums (heads 0,1
+// and 2,3 mod 4), times the key's scale.  Every mode uses this one routine, so
+// a key's logit has the same bits whichever launch computes it.
+__device__ __forceinline__ float lane_logit(uint32_t col, const float4 (&wr)[kHeads / 4], float ksc) {
+  uint64_t acc01 = 0ull, acc23 = 0ull;
+  uint32_t r[16];
+#pragma unroll
+  for (int c = 0; c < kHeads / 16; ++c) {
+    tmem_ld16(col + 16u * c, r);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float4 wv = wr[4 * c + j];
+      acc01 = ffma2(pack2(wv.x, wv.y),
+                    pack2(fmaxf(__uint_as_float(r[4 * j + 0]), 0.f), fmaxf(__uint_as_float(r[4 * j + 1]), 0.f)),
+                    acc01);
+      acc23 = ffma2(pack2(wv.z, wv.w),
+                    pack2(fmaxf(__uint_as_float(r[4 * j + 2]), 0.f), fmaxf(__uint_as_float(r[4 * j + 3]), 0.f)),
+                    acc23);
     }
-    group_bar(q);
-    if (lt < 32) {
-      uint32_t h[8];
-      uint32_t tot = 0;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        h[j] = hist[8 * lane + j];
-        tot += h[j];
-      }
-      uint32_t incl = tot;  // entries in this lane's bins and above
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_down_sync(0xFFFFFFFFu, incl, o);
-        if (lane + o < 32) incl += y;
-      }
-      uint32_t cum = incl - tot;  // entries in higher bins
-#pragma unroll
-      for (int j = 7; j >= 0; --j) {
-        if (cum < kk && cum + h[j] >= kk) {
-          sel[0] = (uint32_t)(8 * lane + j);
-          sel[1] = cum;
-          sel[2] = h[j];
-        }
-        cum += h[j];
-      }
-    }
-    group_bar(q);
-    const uint32_t d = sel[0], above = sel[1], cnt = sel[2];
-    kk -= above;
-    prefix |= (uint64_t)d << shift;
-    mask |= (uint64_t)0xFFu << shift;
-    if (cnt == kk) break;
   }
-  // every thread has read sel before the next call writes it
-  group_bar(q);
-  return prefix;
+  float acc0, acc1, acc2, acc3;
+  unpack2(acc01, acc0, acc1);
+  unpack2(acc23, acc2, acc3);
+  return ((acc0 + acc1) + (acc2 + acc3)) * ksc;
 }
 
-// Keep the Kb best entries of a query's buffer: X = the Kb-th best; entries
-// below X are freed in place (values stay in their record slots) and the
-// free-slot stack is rebuilt in slot order.  Called by the query's 128
-// epilogue threads (lt = 0..127) when the buffer holds more than Kb entries.
-__device__ __noinline__ void fused_compact(uint8_t* qs, int q, int lt, int Kb) {
-  uint64_t* comp = reinterpret_cast<uint64_t*>(qs + kQsComp);
-  uint16_t* freeq = reinterpret_cast<uint16_t*>(qs + kQsFree);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(qs + kQsHist);
-  uint32_t* sel = reinterpret_cast<uint32_t*>(qs + kQsSel);
-  int* cnt = reinterpret_cast<int*>(qs + kQsCnt);
-  uint64_t* tau = reinterpret_cast<uint64_t*>(qs + kQsTau);
-  int* scan = reinterpret_cast<int*>(qs + kQsScan);
-  const uint64_t X = group_kth(comp, kFusedCap, Kb, hist, sel, q, lt);
-  // free slots, ascending: kPer consecutive slots per thread, prefix over 128 threads
-  constexpr int kPer = kFusedCap / 128;
-  int c = 0;
-#pragma unroll
-  for (int i = 0; i < kPer; ++i) {
-    uint64_t& e = comp[kPer * lt + i];
-    if (e < X) e = 0;
-    c += e == 0;
-  }
-  const int lane = lt & 31, wq = lt >> 5;
-  int incl = c;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) scan[wq] = incl;
-  group_bar(q);
-  int pos = incl - c;
-  for (int w = 0; w < wq; ++w) pos += scan[w];
-#pragma unroll
-  for (int i = 0; i < kPer; ++i)
-    if (comp[kPer * lt + i] == 0) freeq[pos++] = (uint16_t)(kPer * lt + i);
-  if (lt == 0) {
-    cnt[0] = 0;
-    *tau = X;
-  }
-  group_bar(q);
+// Gather mode: the listed blocks (and the edge column) of one query, from the
+// record the block top-k wrote.
+struct GatherList {
+  const int32_t* info;  // nullptr when the query needs no values
+  int n;                // listed blocks
+  int groups;           // n + the edge column's group
+  int tiles;
+};
+
+__device__ __forceinline__ GatherList gather_list(const IdxParams& p, int t, bool real) {
+  GatherList g;
+  g.info = nullptr;
+  g.n = g.groups = g.tiles = 0;
+  if (!real) return g;
+  g.info = reinterpret_cast<const int32_t*>(p.ws + (int64_t)t * p.ws_stride + p.info_off);
+  g.n = min(max(g.info[0], 0), p.Kb + 1);  // every index below stays inside the record
+  g.groups = g.n + (g.info[1] ? 1 : 0);
+  g.tiles = (g.groups + kGroupsPerTile - 1) / kGroupsPerTile;
+  return g;
 }
 
-template <bool kFused>
+// First key of group gidx of a query's list: the 8-key group holding listed
+// block info[4 + gidx], or the one holding the edge column S - 1.
+__device__ __forceinline__ int64_t group_first_key(const GatherList& g, int gidx, int B, int64_t S) {
+  const int64_t c = gidx < g.n ? (int64_t)g.info[4 + gidx] * B : S - 1;
+  return c & ~(int64_t)(kGroupRows - 1);
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const IdxParams p) {
@@ -412,19 +326,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int t0 = blockIdx.x * kQueriesPerCta;
   const int nq = min(kQueriesPerCta, p.T - t0);
 
-  // the group's key range: union of its queries' live spans
+  // Tile schedule, the same in every role.  Contiguous modes: tile i holds
+  // keys [klo + 128 i, klo + 128 (i + 1)) of the group's key range (the union
+  // of its queries' live spans).  Gather mode: tiles go round-robin over the
+  // queries; a query's r-th tile holds its groups [16 r, 16 r + 16).
   int64_t klo = INT64_MAX, khi = 0;
-  for (int q = 0; q < nq; ++q) {
-    int64_t s0 = p.starts ? (int64_t)p.starts[t0 + q] : 0;
-    if (s0 < 0) s0 = 0;
-    const int64_t s1 = min((int64_t)p.ends[t0 + q], (int64_t)p.S);
-    if (s1 > s0) {
-      klo = min(klo, s0);
-      khi = max(khi, s1);
+  int ntiles = 0;
+  int qtiles[kQueriesPerCta];  // gather mode: tiles of each query
+  int rounds = 0;
+  if constexpr (kMode == kModeGather) {
+#pragma unroll
+    for (int q = 0; q < kQueriesPerCta; ++q) {
+      qtiles[q] = gather_list(p, t0 + q, q < nq).tiles;
+      ntiles += qtiles[q];
+      rounds = max(rounds, qtiles[q]);
     }
+  } else {
+    for (int q = 0; q < nq; ++q) {
+      int64_t s0 = (kMode == kModeLogits && p.starts) ? (int64_t)p.starts[t0 + q] : 0;
+      if (s0 < 0) s0 = 0;
+      const int64_t s1 = min((int64_t)p.ends[t0 + q], (int64_t)p.S);
+      if (s1 > s0) {
+        klo = min(klo, s0);
+        khi = max(khi, s1);
+      }
+    }
+    if (kMode == kModeBlockMax && khi > 0) klo = 0;  // start 0: blocks align with tiles
+    ntiles = khi > klo ? (int)((khi - klo + kM - 1) / kM) : 0;
   }
-  if (kFused && khi > 0) klo = 0;  // the fused form has start 0: blocks align with tiles
-  const int ntiles = khi > klo ? (int)((khi - klo + kM - 1) / kM) : 0;
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -442,18 +371,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int i = threadIdx.x; i < kQueriesPerCta * kHeads; i += kThreads) {
     const int q = i / kHeads;
     ws[i] = q < nq ? p.w[(int64_t)(t0 + q) * kHeads + (i % kHeads)] : 0.f;
-  }
-  if (kFused) {
-    for (int i = threadIdx.x; i < kQueriesPerCta * kFusedCap; i += kThreads) {
-      uint8_t* qs = base + kOffQs + (i / kFusedCap) * kQsBytes;
-      reinterpret_cast<uint64_t*>(qs + kQsComp)[i % kFusedCap] = 0;
-      reinterpret_cast<uint16_t*>(qs + kQsFree)[i % kFusedCap] = (uint16_t)(i % kFusedCap);
-    }
-    if (threadIdx.x < kQueriesPerCta) {
-      uint8_t* qs = base + kOffQs + threadIdx.x * kQsBytes;
-      reinterpret_cast<int*>(qs + kQsCnt)[0] = 0;
-      *reinterpret_cast<uint64_t*>(qs + kQsTau) = 0;
-    }
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -474,15 +391,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tk) : "memory");
         mbar_expect_tx(qbar, kTileQ);
         tma_load_2d(&tq, qbar, sq, 0, t0 * kHeads);
-        for (int i = 0; i < ntiles; ++i) {
-          const int st = i % kStages;
-          if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) break;
-          mbar_expect_tx(&full[st], kTileK + (i == 0 ? kStarveBytes : 0u));
-          tma_load_2d(&tk, &full[st], sk + st * kTileK, 0, (int)(klo + (int64_t)i * kM));
+        if constexpr (kMode == kModeGather) {
+          int i = 0;
+          bool ok = true;
+          for (int r = 0; r < rounds && ok; ++r) {
+#pragma unroll
+            for (int q = 0; q < kQueriesPerCta; ++q) {
+              if (!ok || r >= qtiles[q]) continue;
+              const int st = i % kStages;
+              if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) {
+                ok = false;
+                continue;
+              }
+              const GatherList g = gather_list(p, t0 + q, true);
+              const int g0 = r * kGroupsPerTile;
+              const int ng = min(kGroupsPerTile, g.groups - g0);
+              mbar_expect_tx(&full[st], (uint32_t)ng * (kGroupRows * kDim) + (i == 0 ? kStarveBytes : 0u));
+              for (int j = 0; j < ng; ++j)
+                tma_load_2d(&tk, &full[st], sk + st * kTileK + j * (kGroupRows * kDim), 0,
+                            (int)group_first_key(g, g0 + j, p.B, p.S));
+              ++i;
+            }
+          }
+        } else {
+          for (int i = 0; i < ntiles; ++i) {
+            const int st = i % kStages;
+            if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) break;
+            mbar_expect_tx(&full[st], kTileK + (i == 0 ? kStarveBytes : 0u));
+            tma_load_2d(&tk, &full[st], sk + st * kTileK, 0, (int)(klo + (int64_t)i * kM));
+          }
         }
       }
     } else if (warp == 1 && lane == 0) {
-      // MMA issuer
+      // MMA issuer: the same instruction sequence in every mode
       if (ntiles > 0 && mbar_wait(qbar, 0)) {
         const uint64_t bdesc = sdesc_sw128(sq);
         for (int i = 0; i < ntiles; ++i) {
@@ -511,7 +452,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = warp & 3;
     const int q = (warp - kCtrlWarps) >> 2;
     const int m = sub * 32 + lane;
-    const int lt = ((warp - kCtrlWarps) & 3) * 32 + lane;  // thread index within the query's group
     const uint32_t lane_addr = tmem + ((uint32_t)(sub * 32) << 16);
     // this warp's query's 64 head weights, held in registers for the whole loop
     float4 wr[kHeads / 4];
@@ -521,124 +461,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     int64_t qs0 = 0, qs1 = 0;
     if (q < nq) {
       const int t = t0 + q;
-      const int64_t a0 = (!kFused && p.starts) ? (int64_t)p.starts[t] : 0;
+      const int64_t a0 = (kMode == kModeLogits && p.starts) ? (int64_t)p.starts[t] : 0;
       qs0 = a0 > 0 ? a0 : 0;
       qs1 = min((int64_t)p.ends[t], (int64_t)p.S);
     }
-    uint8_t* qst = base + kOffQs + q * kQsBytes;
-    const int nbq = (kFused && qs1 > 0) ? (int)((qs1 + p.B - 1) >> p.log2B) : 0;
-    // the tile holding the query's last live block (start 0: klo is 0)
-    const int i_last = nbq > 0 ? (int)(((int64_t)(nbq - 1) << p.log2B) / kM) : -1;
-    // this query's record (only dereferenced for real queries, q < nq)
-    float* rec_vals = reinterpret_cast<float*>(p.ws + (int64_t)(t0 + q) * p.ws_stride + (int64_t)kFusedCap * 8);
-    float* rec_last = rec_vals + (int64_t)kFusedCap * p.B;
-    uint64_t tau = 0;     // insertion threshold: the Kb-th best at the last compaction
-    uint32_t tau_key = 0; // its order key: a block can beat tau only with a key at least this
-    int valid = 0;        // entries kept by the last compaction (0 or Kb)
-    int used = 0;         // this warp's latest view of the insertions since then
-    int64_t s = klo + m;
-    float ksc = s < khi ? p.k_scale[s] : 0.f;
-    for (int i = 0; i < ntiles; ++i, s += kM) {
-      const int a = i & 1;
-      // the next tile's key scale is read while this tile is reduced
-      const int64_t sn = s + kM;
-      const float ksc_next = sn < khi ? p.k_scale[sn] : 0.f;
-      const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&accf[a], (i >> 1) & 1));
-      if (ok) {
-        tc_fence_after();
-        const uint32_t col = lane_addr + (uint32_t)(a * kN + q * kHeads);
-        // 16 heads at a time; two packed partial sums (heads 0,1 and 2,3 mod
-        // 4) keep the FMA chains short.  The order of the sums is fixed, so
-        // both forms produce bit-identical values.
-        uint64_t acc01 = 0ull, acc23 = 0ull;
-        uint32_t r[16];
+    if constexpr (kMode == kModeGather) {
+      float* vals = reinterpret_cast<float*>(p.ws + (int64_t)(t0 + q) * p.ws_stride + p.vals_off);
+      const GatherList mine = gather_list(p, t0 + q, q < nq);
+      int i = 0;
+      for (int r = 0; r < rounds; ++r) {
 #pragma unroll
-        for (int c = 0; c < kHeads / 16; ++c) {
-          tmem_ld16(col + 16u * c, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float4 wv = wr[4 * c + j];
-            acc01 = ffma2(pack2(wv.x, wv.y),
-                          pack2(fmaxf(__uint_as_float(r[4 * j + 0]), 0.f), fmaxf(__uint_as_float(r[4 * j + 1]), 0.f)),
-                          acc01);
-            acc23 = ffma2(pack2(wv.z, wv.w),
-                          pack2(fmaxf(__uint_as_float(r[4 * j + 2]), 0.f), fmaxf(__uint_as_float(r[4 * j + 3]), 0.f)),
-                          acc23);
-          }
-        }
-        float acc0, acc1, acc2, acc3;
-        unpack2(acc01, acc0, acc1);
-        unpack2(acc23, acc2, acc3);
-        const float v = ((acc0 + acc1) + (acc2 + acc3)) * ksc;
-        if constexpr (!kFused) {
-          if (s >= qs0 && s < qs1) p.out[(int64_t)(t0 + q) * p.ld + s] = v;
-        } else {
-          // The query's streaming top-Kb of block maxima.  Most tiles are
-          // settled by one vote: no key of the warp reaches tau's key, so no
-          // block of the warp can enter the buffer.
-          const int Bq = p.B;
-          const uint32_t key = okey(__float_as_uint(v));
-          const bool live = s < qs1;
-          if (__ballot_sync(0xFFFFFFFFu, live && key >= tau_key)) {
-            // block maxima over B consecutive keys (lanes)
-            uint32_t mx = live ? key : 0u;
-            for (int o = 1; o < Bq; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-            const int jb = (int)(s >> p.log2B);
-            const uint64_t c = ocomp(mx, (uint32_t)jb);
-            const bool ins = ((lane & (Bq - 1)) == 0) && live && c > tau;
-            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, ins);
-            if (bal) {
-              int* cnt = reinterpret_cast<int*>(qst + kQsCnt);
-              const int leader = __ffs(bal) - 1;
-              int basei = 0;
-              if (lane == leader) basei = atomicAdd(&cnt[0], __popc(bal));
-              basei = __shfl_sync(0xFFFFFFFFu, basei, leader);
-              used = basei + __popc(bal);
-              int slot = -1;
-              if (ins) {
-                const int idx = basei + __popc(bal & lanemask_lt_u());
-                if (idx < kFusedCap - valid) {
-                  slot = reinterpret_cast<const uint16_t*>(qst + kQsFree)[idx];
-                  reinterpret_cast<uint64_t*>(qst + kQsComp)[slot] = c;
-                } else {
-                  atomicExch(&g_indexer_error, 2);  // unreachable: the capacity checks keep room
-                }
+        for (int tq_ = 0; tq_ < kQueriesPerCta; ++tq_) {
+          if (r >= qtiles[tq_]) continue;
+          const int a = i & 1;
+          const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&accf[a], (i >> 1) & 1));
+          if (ok && tq_ == q) {
+            tc_fence_after();
+            // this row's key: row m % 8 of group m / 8
+            const int gidx = r * kGroupsPerTile + (m >> 3);
+            int64_t key = -1, slot = -1;
+            if (gidx < mine.groups) {
+              key = group_first_key(mine, gidx, p.B, p.S) + (m & (kGroupRows - 1));
+              if (gidx < mine.n) {
+                const int64_t c0 = (int64_t)mine.info[4 + gidx] * p.B;
+                if (key >= 0 && key >= c0 && key < c0 + p.B && key < qs1) slot = (int64_t)gidx * p.B + (key - c0);
+              } else if (key == (int64_t)p.S - 1) {
+                slot = (int64_t)mine.n * p.B;
               }
-              // the block's B values go to its slot of the record
-              const int bslot = __shfl_sync(0xFFFFFFFFu, slot, lane & ~(Bq - 1));
-              if (bslot >= 0) rec_vals[(int64_t)bslot * Bq + (lane & (Bq - 1))] = v;
             }
+            const float ksc = slot >= 0 ? p.k_scale[key] : 0.f;
+            const float v = lane_logit(lane_addr + (uint32_t)(a * kN + q * kHeads), wr, ksc);
+            if (slot >= 0) vals[slot] = v;
           }
-          // the last live block's values, kept whether or not it enters
-          if (i == i_last && (int)(s >> p.log2B) == nbq - 1) rec_last[lane & (Bq - 1)] = v;
+          tc_fence_before();
+          mbar_arrive(&acce[a]);
+          ++i;
         }
       }
-      tc_fence_before();
-      mbar_arrive(&acce[a]);
-      ksc = ksc_next;
-      if constexpr (kFused) {
-        // Capacity check every check_tiles tiles, one reducing barrier.  The
-        // shared counter is only ever raised by atomics, so the warp whose
-        // atomic came last saw the full count and the OR over the group is
-        // exact: all four warps take the same branch.
-        if (((i + 1) & (p.check_tiles - 1)) == 0 && i + 1 < ntiles &&
-            group_any(q, valid + used > kFusedCap - p.check_tiles * (kM >> p.log2B))) {
-          fused_compact(qst, q, lt, p.Kb);
-          tau = *reinterpret_cast<const uint64_t*>(qst + kQsTau);
-          tau_key = (uint32_t)(tau >> 32);
-          valid = p.Kb;
-          used = 0;
+    } else {
+      float* bmax = reinterpret_cast<float*>(p.ws + (int64_t)(t0 + q) * p.ws_stride);
+      int64_t s = klo + m;
+      float ksc = s < khi ? p.k_scale[s] : 0.f;
+      for (int i = 0; i < ntiles; ++i, s += kM) {
+        const int a = i & 1;
+        // the next tile's key scale is read while this tile is reduced
+        const int64_t sn = s + kM;
+        const float ksc_next = sn < khi ? p.k_scale[sn] : 0.f;
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&accf[a], (i >> 1) & 1));
+        if (ok) {
+          tc_fence_after();
+          const float v = lane_logit(lane_addr + (uint32_t)(a * kN + q * kHeads), wr, ksc);
+          if constexpr (kMode == kModeLogits) {
+            if (s >= qs0 && s < qs1) p.out[(int64_t)(t0 + q) * p.ld + s] = v;
+          } else {
+            // the block's largest logit by the total order (B lanes), stored by
+            // its first lane; keys past the live span do not count
+            const bool live = s < qs1;
+            uint32_t mx = live ? okey(__float_as_uint(v)) : 0u;
+            for (int o = 1; o < p.B; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+            if (live && (lane & (p.B - 1)) == 0) bmax[s >> p.log2B] = __uint_as_float(okey_inv(mx));
+          }
         }
-      }
-    }
-    if constexpr (kFused) {
-      // the query's record for the finishing kernel
-      group_bar(q);
-      if (q < nq) {
-        uint64_t* rc = reinterpret_cast<uint64_t*>(p.ws + (int64_t)(t0 + q) * p.ws_stride);
-        const uint64_t* comp = reinterpret_cast<const uint64_t*>(qst + kQsComp);
-        for (int i = lt; i < kFusedCap; i += 128) rc[i] = comp[i];
+        tc_fence_before();
+        mbar_arrive(&acce[a]);
+        ksc = ksc_next;
       }
     }
   }
@@ -694,13 +580,12 @@ int check_cfg(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, co
   return DSA_OK;
 }
 
-template <bool kFused>
+template <int kMode>
 int launch(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const IdxParams& P,
            cudaStream_t stream) {
-  constexpr int smem = kFused ? kSmemFused : kSmemBytes;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(indexer_kernel<kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+    if (cudaFuncSetAttribute(indexer_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
         cudaSuccess) {
       cudaGetLastError();
       return DSA_ERR_CUDA;
@@ -708,10 +593,11 @@ int launch(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const
     configured = true;
   }
   CUtensorMap tq, tk;
-  if (!make_map(&tq, q, (uint64_t)cfg->queries * kHeads, kN) || !make_map(&tk, k, (uint64_t)cfg->keys, kM))
+  const uint32_t box = kMode == kModeGather ? (uint32_t)kGroupRows : (uint32_t)kM;
+  if (!make_map(&tq, q, (uint64_t)cfg->queries * kHeads, kN) || !make_map(&tk, k, (uint64_t)cfg->keys, box))
     return DSA_ERR_CUDA;
   const int grid = (cfg->queries + kQueriesPerCta - 1) / kQueriesPerCta;
-  indexer_kernel<kFused><<<grid, kThreads, smem, stream>>>(tq, tk, P);
+  indexer_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, P);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -738,7 +624,7 @@ int dsa_indexer_logits(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8
   P.ld = cfg->out_stride;
   P.T = cfg->queries;
   P.S = cfg->keys;
-  return launch<false>(cfg, q, k, P, (cudaStream_t)stream);
+  return launch<kModeLogits>(cfg, q, k, P, (cudaStream_t)stream);
 }
 
 int dsa_indexer_select_workspace(const dsa_select_plan* plan, size_t* bytes) {
@@ -748,7 +634,7 @@ int dsa_indexer_select_workspace(const dsa_select_plan* plan, size_t* bytes) {
   int64_t width = 0;
   const int st = dsa_fused_shape(plan, &rows, &width, &B, &Kb);
   if (st != DSA_OK) return st;
-  *bytes = (size_t)rows * (size_t)fused_record_bytes(B);
+  *bytes = (size_t)rows * (size_t)fused_layout(width, B, Kb).bytes;
   return DSA_OK;
 }
 
@@ -765,8 +651,8 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
   if (st != DSA_OK) return st;
   if (cfg->queries != rows || (int64_t)cfg->keys != width) return DSA_ERR_INVALID_ARG;
   if (rows == 0) return DSA_OK;  // keys == width >= 1, so only an empty batch is empty
-  const int64_t rec = fused_record_bytes(B);
-  if (!workspace || (((uintptr_t)workspace) & 15u) || workspace_bytes < (size_t)rows * (size_t)rec ||
+  const FusedLayout L = fused_layout(width, B, Kb);
+  if (!workspace || (((uintptr_t)workspace) & 15u) || workspace_bytes < (size_t)rows * (size_t)L.bytes ||
       !cand || !topk)
     return DSA_ERR_INVALID_ARG;
   IdxParams P;
@@ -778,16 +664,19 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
   P.T = cfg->queries;
   P.S = cfg->keys;
   P.ws = static_cast<uint8_t*>(workspace);
-  P.ws_stride = rec;
+  P.ws_stride = L.bytes;
+  P.info_off = L.info_off;
+  P.vals_off = L.vals_off;
   P.B = B;
   P.log2B = B == 1 ? 0 : B == 2 ? 1 : B == 4 ? 2 : 3;
   P.Kb = Kb;
-  P.check_tiles = kMaxCheckTiles;
-  while (P.check_tiles > 1 && 2 * P.check_tiles * (kM / B) > kFusedCap - kFusedMaxKb) P.check_tiles >>= 1;
-  st = launch<true>(cfg, q, k, P, (cudaStream_t)stream);
-  if (st != DSA_OK) return st;
-  return dsa_fused_finish(plan, static_cast<const uint8_t*>(workspace), rec, ends, cand, topk,
-                          (cudaStream_t)stream);
+  const cudaStream_t s = (cudaStream_t)stream;
+  // 1: block maxima; 2: block top-k and the list of blocks to recompute;
+  // 3: their logits; 4: row top-k
+  if ((st = launch<kModeBlockMax>(cfg, q, k, P, s)) != DSA_OK) return st;
+  if ((st = dsa_fused_blocks(plan, P.ws, ends, cand, s)) != DSA_OK) return st;
+  if ((st = launch<kModeGather>(cfg, q, k, P, s)) != DSA_OK) return st;
+  return dsa_fused_topk(plan, P.ws, ends, cand, topk, s);
 }
 
 }  // extern "C"
@@ -838,7 +727,7 @@ int dsa_indexer_select_noalloc(const dsa_select_plan* plan, const dsa_indexer_cf
   const int st = dsa_fused_shape(plan, &rows, &width, &B, &Kb);
   if (st != DSA_OK) return st;
   // a batch whose records do not fit the fixed array is refused outright
-  if ((uint64_t)rows * (uint64_t)fused_record_bytes(B) > (uint64_t)DSA_NOALLOC_SCRATCH_BYTES)
+  if ((uint64_t)rows * (uint64_t)fused_layout(width, B, Kb).bytes > (uint64_t)DSA_NOALLOC_SCRATCH_BYTES)
     return DSA_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   if (rows > 0) {

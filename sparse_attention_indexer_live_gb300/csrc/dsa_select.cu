@@ -868,58 +868,22 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   }
 }
 
-// Values of the fused indexer selection, from one query's record (start 0):
-// the last live block from its own copy, every other kept block from the
-// streaming slot that holds it.
-struct RecordValues {
-  const uint64_t* comp;  // record: comp[kFusedCap]
-  const float* vals;     // record: vals[kFusedCap << log2B]
-  const float* last;     // record: last[B]
-  int32_t* kslot;        // shared: kslot[j] = slot of block kb[j]
-  const int32_t* kb;
-  int nkb;
-  int64_t last_block;    // n_b - 1
-  int log2B;
-  __device__ void prep(const int32_t* kb_, int nkb_) {
-    kb = kb_;
-    nkb = nkb_;
-    for (int j = threadIdx.x; j < nkb; j += kThreads) kslot[j] = 0;  // every read stays in the record
-    __syncthreads();
-    for (int i = threadIdx.x; i < kFusedCap; i += kThreads) {
-      const uint64_t c = __ldcg(comp + i);
-      if (c == 0) continue;
-      const int32_t b = (int32_t)comp_index(c);
-      const int j = lower_bound_i32(kb, nkb, b);
-      if (j < nkb && kb[j] == b) kslot[j] = i;
-    }
-    __syncthreads();
-  }
-  __device__ __forceinline__ float load(int j, int64_t c) const {
-    const int64_t b = c >> log2B;
-    const int o = (int)(c & ((1 << log2B) - 1));
-    if (b == last_block) return __ldcg(last + o);
-    if (j < 0) j = min(lower_bound_i32(kb, nkb, (int32_t)b), nkb - 1);  // kept blocks are all in kb
-    return __ldcg(vals + ((int64_t)kslot[j] << log2B) + o);
-  }
-};
-
-// Second launch of the fused indexer selection: one CTA per query takes the
-// non-empty slots of the query's record as its streaming buffer, finishes the
-// block top-k exactly as the select kernel does (padding blocks, pin, edge
-// flag, cand) and takes the row top-k from the kept blocks' values.  Nothing
-// is masked: there is no logits row.
-// Dynamic shared memory: bitmap[bitmap_words] u32 | keep[Kb] u64 |
-// kslot[Kb + 1] i32 | region (the larger of the buffer and the row top-k layout)
+// Fused indexer selection, second launch: the block top-k of one query from
+// the block maxima the producer stored in its record (read as one-column
+// blocks, so each carries its block's id), finished exactly as the select
+// kernel finishes (padding blocks, pin, edge flag, cand).  Then the record's
+// list of the blocks whose logits the row top-k will read -- the same list,
+// in the same order, that the row top-k enumerates from cand -- and whether
+// the edge column is read on its own.
+// Dynamic shared memory: the select kernel's layout (bitmap | keep | region).
 __global__ void __launch_bounds__(kThreads, 2)
-    fused_finish_kernel(const Params p, const uint8_t* records, int64_t record_bytes) {
+    fused_blocks_kernel(const Params p, uint8_t* records, int64_t record_bytes, int64_t info_off) {
   extern __shared__ __align__(16) uint8_t dyn[];
   __shared__ Shared sh;
   const int r = blockIdx.x;
   uint32_t* bitmap = reinterpret_cast<uint32_t*>(dyn);
   uint64_t* keep = reinterpret_cast<uint64_t*>(dyn + (((size_t)p.bitmap_words * 4 + 15) & ~(size_t)15));
-  int32_t* kslot = reinterpret_cast<int32_t*>(keep + p.Kb);
-  uint8_t* region = reinterpret_cast<uint8_t*>(kslot) + (((size_t)(p.Kb + 1) * 4 + 15) & ~(size_t)15);
-  uint64_t* buf = reinterpret_cast<uint64_t*>(region);
+  uint64_t* buf = keep + p.Kb;
   for (int i = threadIdx.x; i < p.bitmap_words; i += kThreads) bitmap[i] = 0;
   if (threadIdx.x == 0) {
     sh.cnt = 0;
@@ -927,21 +891,84 @@ __global__ void __launch_bounds__(kThreads, 2)
     sh.edge = 0;
   }
   const Row R = load_row(p, r);
-  const uint8_t* rec = records + (int64_t)r * record_bytes;
-  const uint64_t* comp = reinterpret_cast<const uint64_t*>(rec);
+  uint8_t* rec = records + (int64_t)r * record_bytes;
   __syncthreads();
-  // only ids of live blocks can be in a record; anything else is ignored, so
-  // the bitmap stays in bounds whatever the workspace holds
-  for (int i0 = 0; i0 < kFusedCap; i0 += kThreads) {
-    const int i = i0 + threadIdx.x;
-    const uint64_t c = i < kFusedCap ? __ldcg(comp + i) : 0;
-    warp_append(c != 0 && comp_index(c) < (uint32_t)R.nb, c, buf, &sh.cnt, p.cap);
-  }
+  Params p1 = p;
+  p1.B = 1;
+  p1.log2B = 0;
+  p1.vec_log2g = -1;
+  p1.col_stride = 1;
+  Row R1;
+  R1.s = 0;
+  R1.e = R.nb;
+  R1.ecm = R.nb;
+  R1.L = R.nb;
+  R1.nb = R.nb;
+  stream_block_maxima(p1, reinterpret_cast<const float*>(rec), R1, 0, R.nb, buf, keep, sh);
   __syncthreads();
   finish_block_topk(p, R, r, buf, keep, bitmap, sh);
-  const float* vals = reinterpret_cast<const float*>(rec + (int64_t)kFusedCap * 8);
-  RecordValues src{comp, vals, vals + ((int64_t)kFusedCap << p.log2B), kslot, nullptr, 0, (int64_t)R.nb - 1,
-                   p.log2B};
+  int32_t* info = reinterpret_cast<int32_t*>(rec + info_off);
+  if (R.L <= p.K) {  // the row top-k is the span itself: no logits needed
+    if (threadIdx.x == 0) info[0] = info[1] = 0;
+    return;
+  }
+  const int nkb = min(enumerate_bits(bitmap, R.nb, info + 4, p.Kb + 1, sh), p.Kb + 1);
+  if (threadIdx.x == 0) {
+    const int64_t ec = R.s + R.L;
+    info[0] = nkb;
+    info[1] = (sh.edge && ec == p.width && (p.width - 1) >= R.s && !bit_set(bitmap, R.nb - 1)) ? 1 : 0;
+  }
+}
+
+// Values of the fused form's row top-k: the logits the producer recomputed,
+// block info[4 + j]'s column o at j * B + o, the edge column after them.
+struct CompactValues {
+  const float* vals;
+  const int32_t* kb;
+  int nkb;
+  int B;
+  int log2B;
+  __device__ __forceinline__ void prep(const int32_t* kb_, int nkb_) {
+    kb = kb_;
+    nkb = nkb_;
+  }
+  __device__ __forceinline__ float load(int j, int64_t c) const {
+    if (j < 0) {
+      const int32_t b = (int32_t)(c >> log2B);
+      j = lower_bound_i32(kb, nkb, b);
+      if (j >= nkb || kb[j] != b) return __ldcg(vals + (int64_t)nkb * B);  // the edge column
+    }
+    return __ldcg(vals + (int64_t)j * B + (c & (B - 1)));
+  }
+};
+
+// Fused form, fourth launch: the row top-k from cand and the recomputed
+// logits, as the candidate-mode row top-k does on a masked row.
+// Dynamic shared memory: bitmap[bitmap_words] u32 | candidate layout.
+__global__ void __launch_bounds__(kThreads, 2)
+    fused_topk_kernel(const Params p, const uint8_t* records, int64_t record_bytes, int64_t vals_off) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ Shared sh;
+  const int r = blockIdx.x;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(dyn);
+  uint8_t* region = dyn + (((size_t)p.bitmap_words * 4 + 15) & ~(size_t)15);
+  for (int i = threadIdx.x; i < p.bitmap_words; i += kThreads) bitmap[i] = 0;
+  if (threadIdx.x == 0) sh.edge = 0;
+  const Row R = load_row(p, r);
+  __syncthreads();
+  const int32_t* crow = p.cand_in + (int64_t)r * (p.Kb + 1);
+  for (int i = threadIdx.x; i <= p.Kb; i += kThreads) {
+    const int64_t b = crow[i];
+    if (b < 0) continue;
+    if (R.s + b * p.B < p.width) {
+      atomicOr(&bitmap[b >> 5], 1u << (b & 31));
+    } else {
+      sh.edge = 1;
+    }
+  }
+  __syncthreads();
+  CompactValues src{reinterpret_cast<const float*>(records + (int64_t)r * record_bytes + vals_off), nullptr, 0,
+                    p.B, p.log2B};
   row_topk_kept(p, src, R, r, bitmap, sh.edge != 0, region, sh);
 }
 
@@ -1136,7 +1163,7 @@ struct dsa_select_plan {
   size_t smem_select;
   size_t smem_topk_cand;
   size_t smem_topk_scan;
-  size_t smem_fused;  // fused indexer selection's finishing kernel; 0 = the plan cannot take that form
+  int fused_ok;  // 1 when the plan can take the fused indexer selection
   int ctas_per_sm_select;
 };
 
@@ -1181,17 +1208,12 @@ size_t cand_layout_bytes(const Params& P) {
                  (size_t)(P.K > P.cand_cap ? P.K : P.cand_cap) * 4 + (size_t)P.K * 4);
 }
 
-// Shared memory of the fused form's finishing kernel, or 0 when the plan
-// cannot take the fused form (start 0, one row per bound, unit column stride,
-// a block that fits the producer's lane groups, Kb within its buffer).
-size_t fused_smem(const dsa_select_cfg* c, const Params& P) {
+// Whether a plan can take the fused indexer selection: start 0, one row per
+// bound, unit column stride, a block that divides the producer's 8-key groups.
+bool fusable(const dsa_select_cfg* c) {
   const int B = c->block_size;
-  if (c->has_starts || c->row_repeat != 1 || c->col_stride != 1) return 0;
-  if (!(B == 1 || B == 2 || B == 4 || B == 8) || c->block_topk > kFusedMaxKb) return 0;
-  const size_t buf = (size_t)(kFusedCap + P.Kb) * 8;
-  const size_t cl = cand_layout_bytes(P);
-  return align16((size_t)P.bitmap_words * 4) + align16((size_t)P.Kb * 8) + align16((size_t)(P.Kb + 1) * 4) +
-         (buf > cl ? buf : cl);
+  return !c->has_starts && c->row_repeat == 1 && c->col_stride == 1 &&
+         (B == 1 || B == 2 || B == 4 || B == 8) && B <= kFusedMaxB && c->block_topk <= kFusedMaxKb;
 }
 
 // Shared-memory sizes for a plan whose select kernel runs `split` CTAs per row
@@ -1377,12 +1399,13 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
       rc = DSA_ERR_CUDA;
     }
   }
-  size_t smem_f = rc == DSA_OK ? fused_smem(cfg, P) : 0;
-  if (smem_f && (smem_f + static_smem > (size_t)smem_optin ||
-                 cudaFuncSetAttribute(fused_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      (int)smem_f) != cudaSuccess)) {
+  int fused_ok = rc == DSA_OK && fusable(cfg);
+  if (fused_ok && (cudaFuncSetAttribute(fused_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)z.select) != cudaSuccess ||
+                   cudaFuncSetAttribute(fused_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        (int)z.cand) != cudaSuccess)) {
     cudaGetLastError();
-    smem_f = 0;  // the plan still serves every other call
+    fused_ok = 0;  // the plan still serves every other call
   }
   if (prev >= 0 && prev != device) cudaSetDevice(prev);
   if (rc != DSA_OK) {
@@ -1399,7 +1422,7 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
   pl->smem_select = z.select;
   pl->smem_topk_cand = z.cand;
   pl->smem_topk_scan = z.scan;
-  pl->smem_fused = smem_f;
+  pl->fused_ok = fused_ok;
   pl->ctas_per_sm_select = ctas;
   *plan = pl;
   if (workspace_bytes) *workspace_bytes = 0;
@@ -1517,7 +1540,7 @@ int dsa_combine_window(const dsa_select_plan* plan, const int32_t* starts, const
 
 int dsa_fused_shape(const dsa_select_plan* plan, int32_t* rows, int64_t* width, int32_t* B, int32_t* Kb) {
   if (!plan) return DSA_ERR_INVALID_ARG;
-  if (plan->smem_fused == 0) return DSA_ERR_UNSUPPORTED;
+  if (!plan->fused_ok) return DSA_ERR_UNSUPPORTED;
   *rows = plan->cfg.rows;
   *width = plan->cfg.width;
   *B = plan->cfg.block_size;
@@ -1525,17 +1548,31 @@ int dsa_fused_shape(const dsa_select_plan* plan, int32_t* rows, int64_t* width, 
   return DSA_OK;
 }
 
-int dsa_fused_finish(const dsa_select_plan* plan, const uint8_t* records, int64_t record_bytes,
-                     const int32_t* ends, int32_t* cand, int32_t* topk, cudaStream_t stream) {
-  if (!plan || plan->smem_fused == 0) return DSA_ERR_UNSUPPORTED;
+int dsa_fused_blocks(const dsa_select_plan* plan, uint8_t* records, const int32_t* ends, int32_t* cand,
+                     cudaStream_t stream) {
+  if (!plan || !plan->fused_ok) return DSA_ERR_UNSUPPORTED;
   if (plan->cfg.rows == 0) return DSA_OK;
   Params P = plan->base;
   P.logits = nullptr;
   P.starts = nullptr;
   P.ends = ends;
   P.cand = cand;
+  const FusedLayout L = fused_layout(plan->cfg.width, plan->cfg.block_size, plan->cfg.block_topk);
+  fused_blocks_kernel<<<plan->cfg.rows, kThreads, plan->smem_select, stream>>>(P, records, L.bytes, L.info_off);
+  return finish_launch(cudaSuccess);
+}
+
+int dsa_fused_topk(const dsa_select_plan* plan, const uint8_t* records, const int32_t* ends, const int32_t* cand,
+                   int32_t* topk, cudaStream_t stream) {
+  if (!plan || !plan->fused_ok) return DSA_ERR_UNSUPPORTED;
+  if (plan->cfg.rows == 0) return DSA_OK;
+  Params P = plan->base;
+  P.logits = nullptr;
+  P.starts = nullptr;
+  P.ends = ends;
+  P.cand_in = cand;
   P.topk = topk;
-  P.cap = kFusedCap + P.Kb;
-  fused_finish_kernel<<<plan->cfg.rows, kThreads, plan->smem_fused, stream>>>(P, records, record_bytes);
+  const FusedLayout L = fused_layout(plan->cfg.width, plan->cfg.block_size, plan->cfg.block_topk);
+  fused_topk_kernel<<<plan->cfg.rows, kThreads, plan->smem_topk_cand, stream>>>(P, records, L.bytes, L.vals_off);
   return finish_launch(cudaSuccess);
 }

@@ -83,7 +83,8 @@ def test_edge_ends():
     _run(len(ends), 5000, 8, 32, 64, seed=12, ends=ends)
 
 
-@pytest.mark.parametrize("B,Kb,K", [(1, 40, 128), (2, 100, 300), (4, 256, 700), (8, 1, 16)])
+@pytest.mark.parametrize("B,Kb,K", [(1, 40, 128), (2, 100, 300), (4, 256, 700), (8, 1, 16),
+                                    (1, 1000, 1500)])
 def test_block_sizes(B, Kb, K):
     ends = [3001, 2500, 1, 0, 3001, 64, 1000, 2999, 3005]
     _run(len(ends), 3001, B, Kb, K, seed=13 + B, ends=ends)
@@ -170,7 +171,7 @@ def test_unsupported_and_invalid():
     qd, kd, ksd, wd, end = (torch.from_numpy(x).to(dev) for x in (q, k, ks, w, en))
     cand = torch.empty((T, 33), dtype=torch.int32, device=dev)
     topk = torch.empty((T, 64), dtype=torch.int32, device=dev)
-    for shape in (dict(block_size=16, block_topk=32), dict(block_size=8, block_topk=300),
+    for shape in (dict(block_size=16, block_topk=32), dict(block_size=8, block_topk=32, row_repeat=2),
                   dict(block_size=6, block_topk=32), dict(block_size=8, block_topk=32,
                                                           has_starts=True)):
         plan = dsa.dsa_select_init(rows=T, width=S, row_topk=64, **shape)

@@ -32,7 +32,7 @@ def test_noalloc_matches_the_workspace_call_twice_in_a_row():
     torch = _torch()
     import sparse_attention_indexer_live_gb300 as dsa
     dev = "cuda:0"
-    # 96 queries at block size 8 fit the fixed array (about 7.9 MB of records)
+    # 96 queries of 65,536 keys at block size 8 fit the fixed array (about 4 MB of records)
     T, S, B, Kb, K = 96, 65536, 8, 256, 2048
     plan = dsa.dsa_select_init(rows=T, width=S, block_size=B, block_topk=Kb, row_topk=K)
     need = dsa.dsa_indexer_select_workspace(plan)
@@ -61,7 +61,7 @@ def test_noalloc_refuses_a_batch_larger_than_its_array():
     torch = _torch()
     import sparse_attention_indexer_live_gb300 as dsa
     dev = "cuda:0"
-    T, S = 200, 4096  # 200 records of about 80 KB: more than the 8 MiB array
+    T, S = 40, 1 << 19  # 40 records of about 260 KB: more than the 8 MiB array
     plan = dsa.dsa_select_init(rows=T, width=S, block_size=8, block_topk=32, row_topk=64)
     assert dsa.dsa_indexer_select_workspace(plan) > dsa.NOALLOC_SCRATCH_BYTES
     q, k, ks, w, _, en = wk.indexer_inputs(T, S, seed=34)
