@@ -401,6 +401,7 @@ def measure_extras(dsa, torch, dev, local, prefill):
                                         "achieved_gbs": comb_alg / (us * 1e-6) / 1e9}
     out["indexer_producer"] = measure_producer(dsa, torch, dev)
     out["indexer_select_fused"] = measure_fused(dsa, torch, dev)
+    out["indexer_select_fused_96x1m"] = measure_fused(dsa, torch, dev, T=96, S=1 << 20)
     return out
 
 

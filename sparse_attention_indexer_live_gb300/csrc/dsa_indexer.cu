@@ -40,6 +40,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "dsa_internal.h"
@@ -112,6 +113,7 @@ struct IdxParams {
   int32_t B;       // block size, a power of two <= kFusedMaxB
   int32_t log2B;
   int32_t Kb;      // block top-k: a record lists at most Kb + 1 blocks
+  int32_t nsplit;  // CTAs per group of queries, each an equal share of the key tiles (contiguous modes)
 };
 
 
@@ -323,12 +325,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* ws = reinterpret_cast<float*>(base + kOffW);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t0 = blockIdx.x * kQueriesPerCta;
+  const int grp = blockIdx.x / p.nsplit, part = blockIdx.x - grp * p.nsplit;
+  const int t0 = grp * kQueriesPerCta;
   const int nq = min(kQueriesPerCta, p.T - t0);
 
-  // Tile schedule, the same in every role.  Contiguous modes: tile i holds
-  // keys [klo + 128 i, klo + 128 (i + 1)) of the group's key range (the union
-  // of its queries' live spans).  Gather mode: tiles go round-robin over the
+  // Tile schedule, the same in every role.  Contiguous modes: the group's key
+  // range (the union of its queries' live spans) is cut into 128-key tiles,
+  // nsplit CTAs take an equal share each, and this CTA's tile i holds keys
+  // [klo + 128 i, klo + 128 (i + 1)) with klo the start of its share.  Gather mode: tiles go round-robin over the
   // queries; a query's r-th tile holds its groups [16 r, 16 r + 16).
   int64_t klo = INT64_MAX, khi = 0;
   int ntiles = 0;
@@ -352,7 +356,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (kMode == kModeBlockMax && khi > 0) klo = 0;  // start 0: blocks align with tiles
-    ntiles = khi > klo ? (int)((khi - klo + kM - 1) / kM) : 0;
+    // this CTA's share of the group's tiles (the last shares may be empty)
+    const int total = khi > klo ? (int)((khi - klo + kM - 1) / kM) : 0;
+    const int per = (total + p.nsplit - 1) / p.nsplit;
+    const int tb = min(total, part * per);
+    ntiles = min(total, tb + per) - tb;
+    if (ntiles > 0) klo += (int64_t)tb * kM;
   }
 
   if (threadIdx.x == 0) {
@@ -384,42 +393,51 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < kCtrlWarps) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
-    if (warp == 0 && lane == 0) {
+    if (kMode == kModeGather && warp == 0) {
+      if (ntiles > 0) {
+        // TMA producer, the whole warp: lane j loads group j of a tile
+        if (lane == 0) {
+          asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
+          asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tk) : "memory");
+          mbar_expect_tx(qbar, kTileQ);
+          tma_load_2d(&tq, qbar, sq, 0, t0 * kHeads);
+        }
+        int i = 0;
+        bool ok = true;
+        for (int r = 0; r < rounds && ok; ++r) {
+#pragma unroll
+          for (int q = 0; q < kQueriesPerCta; ++q) {
+            if (!ok || r >= qtiles[q]) continue;
+            const int st = i % kStages;
+            if (i >= kStages && !__all_sync(0xFFFFFFFFu, mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1))) {
+              ok = false;
+              continue;
+            }
+            const GatherList g = gather_list(p, t0 + q, true);
+            const int g0 = r * kGroupsPerTile;
+            const int ng = min(kGroupsPerTile, g.groups - g0);
+            // the stage's byte count is armed before any of its copies can land
+            if (lane == 0) mbar_expect_tx(&full[st], (uint32_t)ng * (kGroupRows * kDim) + (i == 0 ? kStarveBytes : 0u));
+            __syncwarp();
+            if (lane < ng)
+              tma_load_2d(&tk, &full[st], sk + st * kTileK + lane * (kGroupRows * kDim), 0,
+                          (int)group_first_key(g, g0 + lane, p.B, p.S));
+            ++i;
+          }
+        }
+      }
+    } else if (kMode != kModeGather && warp == 0 && lane == 0) {
       if (ntiles > 0) {
         // TMA producer
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tq) : "memory");
         asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tk) : "memory");
         mbar_expect_tx(qbar, kTileQ);
         tma_load_2d(&tq, qbar, sq, 0, t0 * kHeads);
-        if constexpr (kMode == kModeGather) {
-          int i = 0;
-          bool ok = true;
-          for (int r = 0; r < rounds && ok; ++r) {
-#pragma unroll
-            for (int q = 0; q < kQueriesPerCta; ++q) {
-              if (!ok || r >= qtiles[q]) continue;
-              const int st = i % kStages;
-              if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) {
-                ok = false;
-                continue;
-              }
-              const GatherList g = gather_list(p, t0 + q, true);
-              const int g0 = r * kGroupsPerTile;
-              const int ng = min(kGroupsPerTile, g.groups - g0);
-              mbar_expect_tx(&full[st], (uint32_t)ng * (kGroupRows * kDim) + (i == 0 ? kStarveBytes : 0u));
-              for (int j = 0; j < ng; ++j)
-                tma_load_2d(&tk, &full[st], sk + st * kTileK + j * (kGroupRows * kDim), 0,
-                            (int)group_first_key(g, g0 + j, p.B, p.S));
-              ++i;
-            }
-          }
-        } else {
-          for (int i = 0; i < ntiles; ++i) {
-            const int st = i % kStages;
-            if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) break;
-            mbar_expect_tx(&full[st], kTileK + (i == 0 ? kStarveBytes : 0u));
-            tma_load_2d(&tk, &full[st], sk + st * kTileK, 0, (int)(klo + (int64_t)i * kM));
-          }
+        for (int i = 0; i < ntiles; ++i) {
+          const int st = i % kStages;
+          if (i >= kStages && !mbar_wait(&empty[st], ((i / kStages) & 1) ^ 1)) break;
+          mbar_expect_tx(&full[st], kTileK + (i == 0 ? kStarveBytes : 0u));
+          tma_load_2d(&tk, &full[st], sk + st * kTileK, 0, (int)(klo + (int64_t)i * kM));
         }
       }
     } else if (warp == 1 && lane == 0) {
@@ -474,12 +492,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tq_ = 0; tq_ < kQueriesPerCta; ++tq_) {
           if (r >= qtiles[tq_]) continue;
           const int a = i & 1;
-          const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&accf[a], (i >> 1) & 1));
-          if (ok && tq_ == q) {
-            tc_fence_after();
-            // this row's key: row m % 8 of group m / 8
+          // this row's key (row m % 8 of group m / 8) and its scale, read
+          // before the wait so that the load overlaps the MMA
+          int64_t key = -1, slot = -1;
+          float ksc = 0.f;
+          if (tq_ == q) {
             const int gidx = r * kGroupsPerTile + (m >> 3);
-            int64_t key = -1, slot = -1;
             if (gidx < mine.groups) {
               key = group_first_key(mine, gidx, p.B, p.S) + (m & (kGroupRows - 1));
               if (gidx < mine.n) {
@@ -489,7 +507,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 slot = (int64_t)mine.n * p.B;
               }
             }
-            const float ksc = slot >= 0 ? p.k_scale[key] : 0.f;
+            if (slot >= 0) ksc = p.k_scale[key];
+          }
+          const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&accf[a], (i >> 1) & 1));
+          if (ok && tq_ == q) {
+            tc_fence_after();
             const float v = lane_logit(lane_addr + (uint32_t)(a * kN + q * kHeads), wr, ksc);
             if (slot >= 0) vals[slot] = v;
           }
@@ -499,7 +521,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     } else {
-      float* bmax = reinterpret_cast<float*>(p.ws + (int64_t)(t0 + q) * p.ws_stride);
+      // this query's output row: the logits row, or the record's block maxima
+      float* orow = kMode == kModeLogits ? p.out + (int64_t)(t0 + q) * p.ld
+                                         : reinterpret_cast<float*>(p.ws + (int64_t)(t0 + q) * p.ws_stride);
       int64_t s = klo + m;
       float ksc = s < khi ? p.k_scale[s] : 0.f;
       for (int i = 0; i < ntiles; ++i, s += kM) {
@@ -512,14 +536,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const float v = lane_logit(lane_addr + (uint32_t)(a * kN + q * kHeads), wr, ksc);
           if constexpr (kMode == kModeLogits) {
-            if (s >= qs0 && s < qs1) p.out[(int64_t)(t0 + q) * p.ld + s] = v;
+            if (s >= qs0 && s < qs1) orow[s] = v;
           } else {
             // the block's largest logit by the total order (B lanes), stored by
             // its first lane; keys past the live span do not count
             const bool live = s < qs1;
             uint32_t mx = live ? okey(__float_as_uint(v)) : 0u;
-            for (int o = 1; o < p.B; o <<= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-            if (live && (lane & (p.B - 1)) == 0) bmax[s >> p.log2B] = __uint_as_float(okey_inv(mx));
+#pragma unroll
+            for (int o = 1; o < kFusedMaxB; o <<= 1) {
+              const uint32_t y = __shfl_xor_sync(0xFFFFFFFFu, mx, o);
+              if (o < p.B) mx = max(mx, y);
+            }
+            if (live && (lane & (p.B - 1)) == 0) orow[s >> p.log2B] = __uint_as_float(okey_inv(mx));
           }
         }
         tc_fence_before();
@@ -580,9 +608,42 @@ int check_cfg(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, co
   return DSA_OK;
 }
 
+// SM count of the current device, read once per device.
+int sm_count() {
+  static int cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 template <int kMode>
-int launch(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const IdxParams& P,
+int launch(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const IdxParams& P0,
            cudaStream_t stream) {
+  // Few query groups leave SMs idle: split each group's keys over up to
+  // SMs / groups CTAs (one per SM), keeping at least 16 tiles per share.  The
+  // grid depends on the shapes and the device only.
+  IdxParams P = P0;
+  const int groups = (cfg->queries + kQueriesPerCta - 1) / kQueriesPerCta;
+  P.nsplit = 1;
+  if (kMode != kModeGather) {
+    const int sms = sm_count();
+    const int64_t tiles = ((int64_t)cfg->keys + kM - 1) / kM;
+    if (sms > 0 && groups < sms) {
+      const int64_t want = std::min<int64_t>(sms / groups, std::max<int64_t>(1, tiles / 16));
+      P.nsplit = (int)std::max<int64_t>(1, want);
+    }
+  }
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(indexer_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
@@ -596,8 +657,7 @@ int launch(const dsa_indexer_cfg* cfg, const uint8_t* q, const uint8_t* k, const
   const uint32_t box = kMode == kModeGather ? (uint32_t)kGroupRows : (uint32_t)kM;
   if (!make_map(&tq, q, (uint64_t)cfg->queries * kHeads, kN) || !make_map(&tk, k, (uint64_t)cfg->keys, box))
     return DSA_ERR_CUDA;
-  const int grid = (cfg->queries + kQueriesPerCta - 1) / kQueriesPerCta;
-  indexer_kernel<kMode><<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, P);
+  indexer_kernel<kMode><<<groups * P.nsplit, kThreads, kSmemBytes, stream>>>(tq, tk, P);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

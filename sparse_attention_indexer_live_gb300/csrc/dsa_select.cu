@@ -869,9 +869,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
 }
 
 // Fused indexer selection, second launch: the block top-k of one query from
-// the block maxima the producer stored in its record (read as one-column
-// blocks, so each carries its block's id), finished exactly as the select
-// kernel finishes (padding blocks, pin, edge flag, cand).  Then the record's
+// the block maxima the producer stored in its record, finished exactly as the
+// select kernel finishes (padding blocks, pin, edge flag, cand).  Then the record's
 // list of the blocks whose logits the row top-k will read -- the same list,
 // in the same order, that the row top-k enumerates from cand -- and whether
 // the edge column is read on its own.
@@ -893,19 +892,29 @@ __global__ void __launch_bounds__(kThreads, 2)
   const Row R = load_row(p, r);
   uint8_t* rec = records + (int64_t)r * record_bytes;
   __syncthreads();
-  Params p1 = p;
-  p1.B = 1;
-  p1.log2B = 0;
-  p1.vec_log2g = -1;
-  p1.col_stride = 1;
-  Row R1;
-  R1.s = 0;
-  R1.e = R.nb;
-  R1.ecm = R.nb;
-  R1.L = R.nb;
-  R1.nb = R.nb;
-  stream_block_maxima(p1, reinterpret_cast<const float*>(rec), R1, 0, R.nb, buf, keep, sh);
-  __syncthreads();
+  // Streaming top-Kb over the nb maxima, four per 16-byte load and thread per
+  // round.  A round inserts at most 4 * kThreads entries, so compacting while
+  // fewer remain free keeps every append in bounds; the first compaction comes
+  // as soon as 2 * Kb entries are in, so the threshold is set early.
+  const float4* v4 = reinterpret_cast<const float4*>(rec);  // the record is 16-byte aligned
+  const int32_t nb = R.nb;
+  const int32_t nv = (nb + 3) >> 2;
+  for (int32_t v0 = 0; v0 < nv; v0 += kThreads) {
+    if (sh.cnt > p.cap - 4 * kThreads || (sh.tau == 0 && sh.cnt >= 2 * p.Kb))
+      compact_best(buf, keep, p.Kb, p.cap, sh);
+    const uint64_t tau = sh.tau;
+    const int32_t v = v0 + threadIdx.x;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (v < nv) x = __ldcg(v4 + v);
+    const float e[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int32_t j = 4 * v + u;
+      const uint64_t c = compose(order_key(__float_as_uint(e[u])), (uint32_t)j);
+      warp_append(j < nb && c > tau, c, buf, &sh.cnt, p.cap);
+    }
+    __syncthreads();
+  }
   finish_block_topk(p, R, r, buf, keep, bitmap, sh);
   int32_t* info = reinterpret_cast<int32_t*>(rec + info_off);
   if (R.L <= p.K) {  // the row top-k is the span itself: no logits needed
