@@ -30,7 +30,7 @@ def compile_oracle(src: str, out: str) -> str:
     """gcc -O2 a copy of the oracle source into a shared library at `out`."""
     os.makedirs(os.path.dirname(out), exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, src],
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, src, "-lm"],
                    check=True)
     os.replace(tmp, out)
     return out
@@ -68,6 +68,13 @@ def _bind(path: str):
     L.oracle_e4m3.argtypes = [ctypes.c_uint8]
     L.oracle_indexer_logits.restype = ctypes.c_int
     L.oracle_indexer_logits.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, vp, vp, vp, i64]
+    L.oracle_bf16.restype = ctypes.c_double
+    L.oracle_bf16.argtypes = [ctypes.c_uint16]
+    L.oracle_group_union.restype = i32
+    L.oracle_group_union.argtypes = [vp, i32, i32, i32, i32, vp, vp, i32]
+    L.oracle_sparse_attention.restype = ctypes.c_int
+    L.oracle_sparse_attention.argtypes = [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                          ctypes.c_double, vp, vp]
     L.oracle_run.restype = ctypes.c_int
     L.oracle_run.argtypes = [vp, i32, i64, i64, i64, vp, vp, i32, i32, i32, i32, i32, i32,
                              vp, vp]
@@ -174,6 +181,42 @@ class Oracle:
         if rc != OK:
             raise RuntimeError(f"oracle_indexer_logits: {rc}")
         return out
+
+    def bf16(self, b: int) -> float:
+        return float(self.L.oracle_bf16(int(b)))
+
+    def group_union(self, idx, t0, G):
+        """Distinct positions selected by tokens [t0, t0 + G) of idx [T, Kc]
+        (ascending) and, per position, the mask of the tokens that chose it."""
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        T, Kc = idx.shape
+        cap = max(1, G * Kc)
+        keys = np.zeros(cap, dtype=np.int32)
+        mask = np.zeros(cap, dtype=np.uint32)
+        n = self.L.oracle_group_union(idx.ctypes.data, T, Kc, int(t0), int(G), keys.ctypes.data,
+                                      mask.ctypes.data, cap)
+        if n < 0:
+            raise MemoryError
+        return keys[:n], mask[:n]
+
+    def sparse_attention(self, q, k, v, idx, scale):
+        """q [T, H, D], k [S, D], v [S, Dv] as bf16 bit patterns (uint16),
+        idx [T, Kc]; returns (o [T, H, Dv], lse [T, H]) in float64."""
+        q = np.ascontiguousarray(q, dtype=np.uint16)
+        k = np.ascontiguousarray(k, dtype=np.uint16)
+        v = np.ascontiguousarray(v, dtype=np.uint16)
+        idx = np.ascontiguousarray(idx, dtype=np.int32)
+        T, H, D = q.shape
+        S, Dv = v.shape
+        Kc = idx.shape[1]
+        o = np.zeros((T, H, Dv), dtype=np.float64)
+        lse = np.zeros((T, H), dtype=np.float64)
+        rc = self.L.oracle_sparse_attention(q.ctypes.data, k.ctypes.data, v.ctypes.data, idx.ctypes.data,
+                                            T, H, D, Dv, S, Kc, float(scale), o.ctypes.data,
+                                            lse.ctypes.data)
+        if rc != OK:
+            raise RuntimeError(f"oracle_sparse_attention: {rc}")
+        return o, lse
 
     # ---- whole path -----------------------------------------------------
     def row(self, row, width, s, e, B, Kb, K, col_stride=1):

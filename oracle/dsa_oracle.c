@@ -51,6 +51,7 @@
  */
 #include <stdint.h>
 #include <stdlib.h>
+#include <math.h>
 #include <string.h>
 
 #define ORACLE_OK 0
@@ -359,5 +360,112 @@ int oracle_indexer_logits(const uint8_t* q, const uint8_t* k, const float* k_sca
   }
   free(kd);
   free(qd);
+  return ORACLE_OK;
+}
+
+/* ---------------------------------------------------------------------------
+ * NEXT-4: grouped masked sparse attention over the union of neighbouring
+ * queries' selections.
+ *
+ * [P2] vLLM PR #48726, "LiteDSA: grouped masked sparse attention": with H
+ * query heads per token, G = 128 / H adjacent tokens form a group; one GEMM
+ * runs over the union of the group's selected KV positions, and the result
+ * stays query-exact (each token attends to its own selection only).  The
+ * pages fix neither the attention's dimensions nor its formula; the readings
+ * taken (listed in the design notes): multi-query attention in which a
+ * token's H heads share the selected key/value rows, scores scale * q . k,
+ * softmax over the token's selection, the log-sum-exp in natural log; an
+ * empty selection gives o = 0 and lse = -inf.
+ */
+
+/* bf16 bits -> exact double */
+double oracle_bf16(uint16_t b) {
+  uint32_t u = (uint32_t)b << 16;
+  float f;
+  memcpy(&f, &u, sizeof(f));
+  return (double)f;
+}
+
+/* The union of the selections of tokens [t0, min(t0 + G, T)): idx [T, Kc]
+ * rows list positions >= 0 (ascending, -1 padded; any order is accepted).
+ * Writes the distinct positions ascending to keys[] and, for each, the bit
+ * mask of the group's tokens (bit g = token t0 + g) that selected it.
+ * Returns the union size, or ORACLE_ENOMEM when it exceeds cap. */
+int32_t oracle_group_union(const int32_t* idx, int32_t T, int32_t Kc, int32_t t0, int32_t G,
+                           int32_t* keys, uint32_t* mask, int32_t cap) {
+  int32_t n = 0;
+  int32_t t1 = t0 + G < T ? t0 + G : T;
+  for (int32_t t = t0; t < t1; ++t) {
+    for (int32_t i = 0; i < Kc; ++i) {
+      int32_t j = idx[(int64_t)t * Kc + i];
+      if (j < 0) continue;
+      /* position of j in keys[0..n) (kept sorted), by linear search */
+      int32_t p = 0;
+      while (p < n && keys[p] < j) ++p;
+      if (p < n && keys[p] == j) {
+        mask[p] |= 1u << (t - t0);
+        continue;
+      }
+      if (n >= cap) return ORACLE_ENOMEM;
+      for (int32_t r = n; r > p; --r) {
+        keys[r] = keys[r - 1];
+        mask[r] = mask[r - 1];
+      }
+      keys[p] = j;
+      mask[p] = 1u << (t - t0);
+      ++n;
+    }
+  }
+  return n;
+}
+
+/* Attention of every token over its own selection, in double precision:
+ * q [T, H, D], k [S, D], v [S, Dv] (bf16 bits), idx [T, Kc]; o [T, H, Dv],
+ * lse [T, H].  Positions outside [0, S) are an error. */
+int oracle_sparse_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, const int32_t* idx,
+                            int32_t T, int32_t H, int32_t D, int32_t Dv, int32_t S, int32_t Kc, double scale,
+                            double* o, double* lse) {
+  double* s = (double*)malloc((size_t)(Kc > 0 ? Kc : 1) * sizeof(double));
+  if (!s) return ORACLE_ENOMEM;
+  for (int32_t t = 0; t < T; ++t) {
+    for (int32_t h = 0; h < H; ++h) {
+      const uint16_t* qh = q + ((int64_t)t * H + h) * D;
+      double* oh = o + ((int64_t)t * H + h) * Dv;
+      for (int32_t c = 0; c < Dv; ++c) oh[c] = 0.0;
+      double m = -INFINITY;
+      int32_t n = 0;
+      for (int32_t i = 0; i < Kc; ++i) {
+        int32_t j = idx[(int64_t)t * Kc + i];
+        if (j < 0) {
+          s[i] = -INFINITY;
+          continue;
+        }
+        if (j >= S) {
+          free(s);
+          return ORACLE_EINVAL;
+        }
+        double dot = 0.0;
+        for (int32_t d = 0; d < D; ++d) dot += oracle_bf16(qh[d]) * oracle_bf16(k[(int64_t)j * D + d]);
+        s[i] = scale * dot;
+        if (s[i] > m) m = s[i];
+        ++n;
+      }
+      if (n == 0) {
+        lse[(int64_t)t * H + h] = -INFINITY;
+        continue;
+      }
+      double l = 0.0;
+      for (int32_t i = 0; i < Kc; ++i) {
+        int32_t j = idx[(int64_t)t * Kc + i];
+        if (j < 0) continue;
+        double p = exp(s[i] - m);
+        l += p;
+        for (int32_t c = 0; c < Dv; ++c) oh[c] += p * oracle_bf16(v[(int64_t)j * Dv + c]);
+      }
+      for (int32_t c = 0; c < Dv; ++c) oh[c] /= l;
+      lse[(int64_t)t * H + h] = m + log(l);
+    }
+  }
+  free(s);
   return ORACLE_OK;
 }

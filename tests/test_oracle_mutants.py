@@ -8,6 +8,7 @@ import pytest
 
 import oracle
 from tests import test_combine_window as combine
+from tests import test_oracle_attention as att
 from tests import test_oracle_pins as pins
 from tests.common import load_golden
 
@@ -39,6 +40,13 @@ MUTANTS = [
      "int64_t w0 = w1 - window + 1 > s ? w1 - window + 1 : s;"),
     ("combine_keeps_duplicates", "if (m == 0 || all[i] != all[m - 1]) all[m++] = all[i];",
      "all[m++] = all[i];"),
+    ("attention_counts_instead_of_weights", "        l += p;\n", "        l += 1.0;\n"),
+    ("lse_without_max", "lse[(int64_t)t * H + h] = m + log(l);", "lse[(int64_t)t * H + h] = log(l);"),
+    ("union_mask_absolute_bit", "mask[p] |= 1u << (t - t0);", "mask[p] |= 1u << t;"),
+    ("bf16_wrong_shift", "uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;"),
+    ("score_without_scale", "s[i] = scale * dot;", "s[i] = dot;"),
+    ("union_drops_last_token", "int32_t t1 = t0 + G < T ? t0 + G : T;",
+     "int32_t t1 = t0 + G - 1 < T ? t0 + G - 1 : T;"),
 ]
 
 
@@ -57,6 +65,13 @@ def _pins_fail(orc) -> list:
         ("brute_repeat", lambda: pins.test_brute_force_row_repeat(orc)),
         ("b1_reduction", lambda: pins.test_b1_reduces_to_stable_topk(orc)),
         ("invariants", lambda: pins.test_invariants_and_idempotence_random(orc)),
+        ("att_bf16", lambda: att.test_bf16_decoding(orc)),
+        ("att_single", lambda: att.test_single_position_is_that_row(orc)),
+        ("att_equal", lambda: att.test_equal_scores_average_the_values(orc)),
+        ("att_numpy", lambda: att.test_matches_an_independent_numpy_softmax(orc)),
+        ("att_order", lambda: att.test_order_and_padding_do_not_matter(orc)),
+        ("att_empty", lambda: att.test_empty_selection(orc)),
+        ("att_union", lambda: att.test_union_against_sets(orc)),
     ]
     for name, fn in checks:
         try:

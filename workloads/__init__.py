@@ -294,3 +294,55 @@ def indexer_inputs(T: int, S: int, seed: int = 7, heads: int = 64, dim: int = 12
     else:
         ends = np.full(T, S, dtype=np.int32)
     return q, k, ks, w, None, ends
+
+
+# ---------------------------------------------------------------------------
+# grouped sparse attention (NEXT-4) inputs
+
+_S_AQ = 121
+_S_AK = 122
+_S_AV = 123
+_S_ASEL = 124
+_S_ATOK = 125
+
+
+def bf16_normal(seed: int, stream: int, n: int, scale: float = 1.0) -> np.ndarray:
+    """n N(0, scale^2) values (Box-Muller on Philox words) rounded to bf16,
+    returned as their 16-bit patterns (round to nearest, ties to even)."""
+    a = u32(seed, stream, 0, 2 * n)
+    u1, u2 = _unit(a[0::2]), _unit(a[1::2])
+    x = (scale * np.sqrt(-2.0 * np.log(u1)) * np.cos(2.0 * math.pi * u2)).astype(np.float32)
+    u = x.view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def attention_inputs(T: int, H: int, S: int, Kc: int, seed: int = 9, dim: int = 128, G: int = 16,
+                     own: float = 0.1, fill: float = 1.0):
+    """(q [T, H, dim], k [S, dim], v [S, dim] as bf16 bits, idx [T, Kc]).
+
+    Neighbouring tokens select overlapping positions, as the pages observe:
+    the tokens of each group of G share a base selection of Kc positions and
+    each replaces a fraction `own` of it with positions of its own.  A token
+    selects round(fill * Kc) positions (ascending, distinct, -1 padded);
+    scores are kept moderate by a 1/4 spread on q."""
+    q = bf16_normal(seed, _S_AQ, T * H * dim, 0.25).reshape(T, H, dim)
+    k = bf16_normal(seed, _S_AK, S * dim).reshape(S, dim)
+    v = bf16_normal(seed, _S_AV, S * dim).reshape(S, dim)
+    idx = np.full((T, Kc), -1, dtype=np.int32)
+    n = max(0, min(int(round(fill * Kc)), S))
+    for g0 in range(0, T, G):
+        base = u32(seed, _S_ASEL, g0, 4 * Kc + 64) % max(S, 1)
+        base = np.unique(base)[:n] if n else base[:0]
+        for t in range(g0, min(g0 + G, T)):
+            r = u32(seed, _S_ATOK, t, 2 * Kc + 8)
+            sel = base.copy()
+            m = int(own * len(sel))
+            if m:
+                swap = np.unique(r[:m] % len(sel))
+                sel[swap] = r[Kc:Kc + len(swap)] % S
+            sel = np.unique(sel)
+            # refill to n distinct positions if replacements collided
+            extra = r[Kc + m:] % S
+            sel = np.unique(np.concatenate([sel, extra]))[:n] if len(sel) < n else sel[:n]
+            idx[t, :len(sel)] = np.sort(sel)
+    return q, k, v, idx
