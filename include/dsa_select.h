@@ -238,6 +238,61 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
                        struct CUstream_st* stream);
 
 /*
+ * Grouped masked sparse attention over the selection.
+ *
+ * vLLM PR #48726 ("LiteDSA: grouped masked sparse attention"): with H query
+ * heads per token, G = 128 / H adjacent tokens form a group whose G x H
+ * query/head rows fill one 128-row tensor-core tile; one GEMM runs over the
+ * union of the group's selected KV positions, and each token still attends to
+ * its own selection only.  The pages fix neither the dimensions nor the
+ * formula; this build takes multi-query attention (a token's heads share the
+ * selected key and value rows): for token t, head h and its selection A(t),
+ *     o[t, h] = sum_{j in A(t)} softmax_j(scale * q[t, h] . k[j]) v[j]
+ *     lse[t, h] = ln sum_{j in A(t)} exp(scale * q[t, h] . k[j])
+ * and an empty A(t) gives o = 0, lse = -inf.
+ *   heads      8 or 16 (G = 16 or 8);  head_dim = value_dim = 128
+ *   keys       S <= 2^20 (the union is built in a bitmap of the key range)
+ *   select     Kc: entries per token in idx
+ *   idx        int32 [tokens, Kc]: each row's positions in [0, S), distinct,
+ *              any order, -1 for unused entries (dsa_row_topk and
+ *              dsa_combine_window rows qualify)
+ *   q          bf16 [tokens, heads, 128];  k, v  bf16 [keys, 128]
+ *   o          f32 [tokens, heads, 128];  lse  f32 [tokens, heads]
+ *   workspace  device memory, 16-byte aligned, of at least
+ *              dsa_sparse_attention_workspace() bytes; per group of G tokens:
+ *              n (int32, padded to 16 bytes) | keys[G * Kc] int32, the union
+ *              ascending | masks[G * Kc] uint32, bit g set when token
+ *              group * G + g selected that position
+ */
+typedef struct dsa_attention_cfg {
+  int32_t tokens;
+  int32_t heads;
+  int32_t keys;
+  int32_t head_dim;
+  int32_t value_dim;
+  int32_t select;
+} dsa_attention_cfg;
+
+int dsa_sparse_attention_workspace(const dsa_attention_cfg* cfg, size_t* bytes);
+
+/* Only the unions and masks, into workspace (the first launch of
+ * dsa_sparse_attention). */
+int dsa_group_union(const dsa_attention_cfg* cfg, const int32_t* idx, void* workspace,
+                    size_t workspace_bytes, struct CUstream_st* stream);
+
+/* The unions, then the attention (tcgen05, bf16 operands, fp32 accumulation;
+ * P is rounded to bf16 for the P V product).  scale: the softmax scale, e.g.
+ * 1/sqrt(128).  q, k, v, o 16-byte aligned; v finite.  Bounded-wait timeouts
+ * are reported by dsa_sparse_attention_status(). */
+int dsa_sparse_attention(const dsa_attention_cfg* cfg, const uint16_t* q, const uint16_t* k,
+                         const uint16_t* v, const int32_t* idx, float scale, void* workspace,
+                         size_t workspace_bytes, float* o, float* lse, struct CUstream_st* stream);
+
+/* DSA_ERR_TIMEOUT once after an attention launch gave up a wait (then
+ * cleared), else DSA_OK; synchronises the device. */
+int dsa_sparse_attention_status(void);
+
+/*
  * dsa_indexer_select without a caller workspace: the fused producer +
  * selection, with its per-query records kept in one fixed array inside this
  * library instead of memory the caller allocates.  The pages describe nothing

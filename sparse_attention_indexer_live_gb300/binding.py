@@ -38,7 +38,8 @@ class dsa_plan_desc(ctypes.Structure):
 EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_candidate_select",
            "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_indexer_logits",
            "dsa_indexer_status", "dsa_indexer_select_workspace", "dsa_indexer_select",
-           "dsa_indexer_select_noalloc", "dsa_status_string")
+           "dsa_indexer_select_noalloc", "dsa_sparse_attention_workspace", "dsa_group_union",
+           "dsa_sparse_attention", "dsa_sparse_attention_status", "dsa_status_string")
 
 # Size of the library's fixed scratch array used by dsa_indexer_select_noalloc
 # (DSA_NOALLOC_SCRATCH_BYTES in include/dsa_select.h).
@@ -48,6 +49,11 @@ NOALLOC_SCRATCH_BYTES = 8 << 20
 class dsa_indexer_cfg(ctypes.Structure):
     _fields_ = [("queries", ctypes.c_int32), ("keys", ctypes.c_int32), ("heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("out_stride", ctypes.c_int64)]
+
+class dsa_attention_cfg(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int32), ("heads", ctypes.c_int32), ("keys", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("value_dim", ctypes.c_int32), ("select", ctypes.c_int32)]
+
 
 _lib = None
 _lock = threading.Lock()
@@ -95,6 +101,16 @@ def load(path: str | None = None):
             L.dsa_indexer_select.restype = i32
             L.dsa_indexer_select.argtypes = [vp, ctypes.POINTER(dsa_indexer_cfg), vp, vp, vp, vp,
                                              vp, vp, ctypes.c_size_t, vp, vp, vp]
+            L.dsa_sparse_attention_workspace.restype = i32
+            L.dsa_sparse_attention_workspace.argtypes = [ctypes.POINTER(dsa_attention_cfg),
+                                                         ctypes.POINTER(ctypes.c_size_t)]
+            L.dsa_group_union.restype = i32
+            L.dsa_group_union.argtypes = [ctypes.POINTER(dsa_attention_cfg), vp, vp, ctypes.c_size_t, vp]
+            L.dsa_sparse_attention.restype = i32
+            L.dsa_sparse_attention.argtypes = [ctypes.POINTER(dsa_attention_cfg), vp, vp, vp, vp,
+                                               ctypes.c_float, vp, ctypes.c_size_t, vp, vp, vp]
+            L.dsa_sparse_attention_status.restype = i32
+            L.dsa_sparse_attention_status.argtypes = []
             L.dsa_indexer_select_noalloc.restype = i32
             L.dsa_indexer_select_noalloc.argtypes = [vp, ctypes.POINTER(dsa_indexer_cfg), vp, vp, vp,
                                                      vp, vp, vp, vp, vp]
@@ -318,6 +334,51 @@ def dsa_indexer_select_noalloc(plan: Plan, q, k, k_scale, w, ends, cand, topk, s
                                              _ptr(k_scale), _ptr(w), _ptr(ends), _ptr(cand),
                                              _ptr(topk), _stream(stream)),
            f"dsa_indexer_select_noalloc (fixed scratch of {NOALLOC_SCRATCH_BYTES} bytes)")
+
+
+def attention_cfg(q, k, idx) -> dsa_attention_cfg:
+    T, H, D = q.shape
+    return dsa_attention_cfg(tokens=T, heads=H, keys=k.shape[0], head_dim=D, value_dim=D,
+                             select=idx.shape[1])
+
+
+def dsa_sparse_attention_workspace(cfg: dsa_attention_cfg) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().dsa_sparse_attention_workspace(ctypes.byref(cfg), ctypes.byref(n)),
+           "dsa_sparse_attention_workspace")
+    return int(n.value)
+
+
+def dsa_group_union(cfg: dsa_attention_cfg, idx, workspace, stream=None):
+    """The unions of each group's selections and their token masks, written
+    to workspace (layout in include/dsa_select.h)."""
+    import torch
+    assert idx.dtype == torch.int32 and idx.is_cuda and idx.is_contiguous(), "idx"
+    assert workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace"
+    _check(load().dsa_group_union(ctypes.byref(cfg), _ptr(idx), _ptr(workspace), workspace.numel(),
+                                  _stream(stream)), "dsa_group_union")
+
+
+def dsa_sparse_attention(cfg: dsa_attention_cfg, q, k, v, idx, scale: float, workspace, o, lse,
+                         stream=None):
+    """Grouped masked sparse attention: q [T, H, 128], k / v [S, 128] as bf16
+    tensors (or their uint16 bit patterns), idx [T, Kc] int32; writes o
+    [T, H, 128] and lse [T, H] (float32)."""
+    import torch
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        assert t.dtype in (torch.bfloat16, torch.uint16, torch.int16) and t.is_cuda and \
+            t.is_contiguous(), name
+    assert idx.dtype == torch.int32 and idx.is_cuda and idx.is_contiguous(), "idx"
+    for name, t in (("o", o), ("lse", lse)):
+        assert t.dtype == torch.float32 and t.is_cuda and t.is_contiguous(), name
+    assert workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace"
+    _check(load().dsa_sparse_attention(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx),
+                                       float(scale), _ptr(workspace), workspace.numel(), _ptr(o),
+                                       _ptr(lse), _stream(stream)), "dsa_sparse_attention")
+
+
+def dsa_sparse_attention_status() -> int:
+    return int(load().dsa_sparse_attention_status())
 
 
 def dsa_indexer_status() -> int:

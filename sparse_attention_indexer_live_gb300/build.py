@@ -12,7 +12,8 @@ import subprocess
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
-SOURCES = [os.path.join(PKG, "csrc", "dsa_select.cu"), os.path.join(PKG, "csrc", "dsa_indexer.cu")]
+SOURCES = [os.path.join(PKG, "csrc", "dsa_select.cu"), os.path.join(PKG, "csrc", "dsa_indexer.cu"),
+           os.path.join(PKG, "csrc", "dsa_attention.cu")]
 HEADERS = [os.path.join(INCLUDE, "dsa_select.h"), os.path.join(PKG, "csrc", "dsa_internal.h")]
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libdsa_select.so")

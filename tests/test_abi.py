@@ -137,3 +137,24 @@ def test_product_path_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in src.replace("the oracle", ""), f
+
+
+def test_attention_shapes_checked_without_cuda(lib):
+    # the workspace query validates the shape on the host only
+    def ws(**kw):
+        c = dict(tokens=37, heads=8, keys=5000, head_dim=128, value_dim=128, select=64)
+        c.update(kw)
+        n = ctypes.c_size_t(123)
+        rc = lib.dsa_sparse_attention_workspace(ctypes.byref(binding.dsa_attention_cfg(**c)), ctypes.byref(n))
+        return rc, n.value
+    rc, n = ws()
+    # 3 groups of 16 tokens: header 16 + keys 16 * 64 * 4 + masks 16 * 64 * 4 bytes each
+    assert rc == dsa.DSA_OK and n == 3 * (16 + 2 * 16 * 64 * 4)
+    rc, n = ws(heads=16)
+    assert rc == dsa.DSA_OK and n == 5 * (16 + 2 * 8 * 64 * 4)
+    for kw in (dict(heads=4), dict(heads=32), dict(head_dim=64), dict(value_dim=256),
+               dict(keys=(1 << 20) + 1)):
+        assert ws(**kw)[0] == dsa.DSA_ERR_UNSUPPORTED, kw
+    for kw in (dict(tokens=-1), dict(select=-2), dict(keys=-5)):
+        assert ws(**kw)[0] == dsa.DSA_ERR_INVALID_ARG, kw
+    assert lib.dsa_sparse_attention_workspace(None, ctypes.byref(ctypes.c_size_t())) == dsa.DSA_ERR_INVALID_ARG

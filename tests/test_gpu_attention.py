@@ -1,0 +1,135 @@
+"""Grouped masked sparse attention on the GPU (dsa_group_union,
+dsa_sparse_attention) against the oracle: the unions and masks exactly, the
+outputs within a bound derived from the arithmetic.
+
+Bound: q, k, v are bf16 (exact in the oracle's doubles).  The scores come
+from fp32 tensor-core accumulation (relative error far below 2^-16 of
+sum |q||k|); the softmax weights p are computed in fp32 and rounded to bf16
+(relative error <= 2^-9) for the P V product, whose fp32 accumulation adds
+far less.  o is a weighted mean of value rows, so |o - o_exact| <=
+2^-9 * max_j |v_j| + the score error's effect; the test allows 2^-8 *
+max_j |v_j| + 1e-5.  lse uses the unrounded fp32 weights: |error| <= 1e-4 +
+1e-5 |lse|.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import workloads as wk
+from oracle import default as oracle_default
+
+pytestmark = pytest.mark.gpu
+
+
+def _torch():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    return torch
+
+
+def _f(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _union_from_ws(ws_np, G, Kc, groups):
+    cap = G * Kc
+    keys_off = 16
+    masks_off = keys_off + ((cap * 4 + 15) & ~15)
+    rec = masks_off + ((cap * 4 + 15) & ~15)
+    out = []
+    for g in range(groups):
+        r = ws_np[g * rec:(g + 1) * rec]
+        n = int(r[:4].view(np.int32)[0])
+        keys = r[keys_off:keys_off + 4 * n].view(np.int32)
+        masks = r[masks_off:masks_off + 4 * n].view(np.uint32)
+        out.append((keys, masks))
+    return out
+
+
+def _run(T, H, S, Kc, seed, own=0.1, fill=1.0, idx_fn=None, check_union=True):
+    torch = _torch()
+    import sparse_attention_indexer_live_gb300 as dsa
+    q, k, v, idx = wk.attention_inputs(T, H, S, Kc, seed=seed, own=own, fill=fill, G=128 // H)
+    if idx_fn is not None:
+        idx = idx_fn(idx)
+    dev = "cuda:0"
+    qd, kd, vd, idd = (torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).to(dev)
+                       for x in (q, k, v, idx))
+    cfg = dsa.attention_cfg(qd, kd, idd)
+    ws = torch.zeros(dsa.dsa_sparse_attention_workspace(cfg), dtype=torch.uint8, device=dev)
+    o = torch.full((T, H, 128), 7.0, dtype=torch.float32, device=dev)
+    lse = torch.full((T, H), 7.0, dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(128)
+    dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse)
+    torch.cuda.synchronize()
+    assert dsa.dsa_sparse_attention_status() == dsa.DSA_OK
+    orc = oracle_default()
+    G = 128 // H
+    groups = -(-T // G)
+    if check_union:
+        got = _union_from_ws(ws.cpu().numpy(), G, Kc, groups)
+        for g in range(groups):
+            keys, masks = orc.group_union(idx, g * G, G)
+            assert np.array_equal(got[g][0], keys), f"union keys of group {g}"
+            assert np.array_equal(got[g][1], masks), f"union masks of group {g}"
+    o_ref, lse_ref = orc.sparse_attention(q, k, v, idx, scale)
+    og, lg = o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+    vf = _f(v)
+    for t in range(T):
+        sel = idx[t][idx[t] >= 0]
+        if len(sel) == 0:
+            assert np.all(og[t] == 0.0) and np.all(np.isneginf(lg[t])), f"token {t} (empty)"
+            continue
+        vmax = np.abs(vf[sel]).max()
+        err = np.abs(og[t] - o_ref[t]).max()
+        assert err <= 2.0 ** -8 * vmax + 1e-5, f"token {t}: o error {err} vs bound {2.0 ** -8 * vmax}"
+        lerr = np.abs(lg[t] - lse_ref[t])
+        assert np.all(lerr <= 1e-4 + 1e-5 * np.abs(lse_ref[t])), f"token {t}: lse error {lerr.max()}"
+    return og, lg
+
+
+def test_union_and_attention_small():
+    # 37 tokens (a ragged last group), one 128-position tile or two per group
+    _run(37, 8, 5000, 64, seed=1)
+
+
+def test_sixteen_heads():
+    _run(29, 16, 3000, 100, seed=2)
+
+
+def test_many_tiles_and_low_overlap():
+    # large unions: 16 tokens x 300 positions with 40 % of each token's own
+    _run(40, 8, 60000, 300, seed=3, own=0.4)
+
+
+def test_edge_selections():
+    def f(idx):
+        idx = idx.copy()
+        idx[3] = -1                       # nothing selected
+        idx[4] = -1
+        idx[4, 0] = 17                    # one position
+        idx[5, ::2] = -1                  # holes inside the row
+        idx[20] = -1
+        idx[20, :3] = [0, 4999, 2500]     # first and last key, unsorted
+        return idx
+    _run(33, 8, 5000, 48, seed=4, idx_fn=f)
+
+
+def test_full_key_range_and_wide_selection():
+    # keys at the 2^20 limit and 2048-entry selections (the row top-k's size)
+    _run(32, 8, 1 << 20, 2048, seed=5, own=0.05)
+
+
+def test_unsupported_shapes():
+    torch = _torch()
+    import sparse_attention_indexer_live_gb300 as dsa
+    n = torch.empty(1)
+    for kw in (dict(heads=4), dict(head_dim=64), dict(keys=(1 << 20) + 1)):
+        c = dict(tokens=8, heads=8, keys=1000, head_dim=128, value_dim=128, select=16)
+        c.update(kw)
+        with pytest.raises(dsa.DsaSelectError) as e:
+            dsa.dsa_sparse_attention_workspace(dsa.dsa_attention_cfg(**c))
+        assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
+    del n
