@@ -17,6 +17,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -402,6 +403,7 @@ def measure_extras(dsa, torch, dev, local, prefill):
     out["indexer_producer"] = measure_producer(dsa, torch, dev)
     out["indexer_select_fused"] = measure_fused(dsa, torch, dev)
     out["indexer_select_fused_96x1m"] = measure_fused(dsa, torch, dev, T=96, S=1 << 20)
+    out["grouped_sparse_attention"] = measure_attention(dsa, torch, dev)
     return out
 
 
@@ -480,6 +482,49 @@ def measure_fused(dsa, torch, dev, T=608, S=131072, B=8, Kb=256, K=2048):
     res["same_result"] = bool(torch.equal(cand, cand2) and torch.equal(topk, topk2))
     res["status"] = dsa.dsa_indexer_status()
     return res
+
+
+def measure_attention(dsa, torch, dev, T=2048, H=8, S=1 << 20, Kc=2048, own=0.05):
+    """Grouped masked sparse attention (dsa_sparse_attention): union build plus
+    attention, on T tokens whose neighbours share most of their selection."""
+    q, k, v, idx = wk.attention_inputs(T, H, S, Kc, seed=21, own=own, G=128 // H)
+    qd, kd, vd = (torch.from_numpy(x.view(np.int16)).to(dev) for x in (q, k, v))
+    idd = torch.from_numpy(idx).to(dev)
+    cfg = dsa.attention_cfg(qd, kd, idd)
+    ws = torch.zeros(dsa.dsa_sparse_attention_workspace(cfg), dtype=torch.uint8, device=dev)
+    o = torch.empty((T, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(128)
+    for _ in range(3):
+        dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse)
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    for _ in range(10):
+        dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse)
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / 10
+    G = 128 // H
+    groups = -(-T // G)
+    cap = G * Kc
+    rec = 16 + 2 * ((cap * 4 + 15) & ~15)
+    wsn = ws.cpu().numpy()
+    union = np.array([int(wsn[g * rec:g * rec + 4].view(np.int32)[0]) for g in range(groups)])
+    sel = (idx >= 0).sum(axis=1)
+    useful = 2.0 * H * float(sel.sum()) * (128 + 128)
+    tiles = np.ceil(union / 128.0)
+    executed = 2.0 * groups * 128 * float((tiles * 128).sum() / groups) * (128 + 128)
+    peak = None
+    try:
+        with open(PEAKS) as f:
+            peak = float(json.load(f)["bf16_tflops"])
+    except Exception:
+        peak = 1900.0
+    return {"tokens": T, "heads": H, "group": G, "keys": S, "select": Kc, "neighbour_own_fraction": own,
+            "us_per_call": us, "tokens_per_s": T / (us * 1e-6),
+            "union_over_selection": float(union.mean() / sel.mean()),
+            "useful_tflops": useful / (us * 1e-6) / 1e12, "executed_tflops": executed / (us * 1e-6) / 1e12,
+            "bf16_peak_tflops": peak, "status": dsa.dsa_sparse_attention_status()}
 
 
 # ---------------------------------------------------------------------------
@@ -625,6 +670,8 @@ def main():
                     help="time only the tensor-core indexer-logits producer and print its JSON")
     ap.add_argument("--fused-only", nargs=2, type=int, metavar=("QUERIES", "KEYS"),
                     help="time only the fused producer + selection against the two-step path")
+    ap.add_argument("--attention-only", action="store_true",
+                    help="time only the grouped masked sparse attention and print its JSON")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the supplementary decode / single-row / scan-mode timings")
     ap.add_argument("--rows", type=int, default=None,
@@ -634,6 +681,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 1:
         ap.error("--warmup must be >= 1")
+    if args.attention_only:
+        import torch
+
+        import sparse_attention_indexer_live_gb300 as dsa
+        dsa.build()
+        dsa.load()
+        print(json.dumps(measure_attention(dsa, torch, torch.device("cuda:0"))), flush=True)
+        return
     if args.producer_only or args.fused_only:
         import torch
 

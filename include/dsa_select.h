@@ -251,11 +251,12 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
  *     lse[t, h] = ln sum_{j in A(t)} exp(scale * q[t, h] . k[j])
  * and an empty A(t) gives o = 0, lse = -inf.
  *   heads      8 or 16 (G = 16 or 8);  head_dim = value_dim = 128
- *   keys       S <= 2^20 (the union is built in a bitmap of the key range)
- *   select     Kc: entries per token in idx
- *   idx        int32 [tokens, Kc]: each row's positions in [0, S), distinct,
- *              any order, -1 for unused entries (dsa_row_topk and
- *              dsa_combine_window rows qualify)
+ *   keys       S: rows of k and v
+ *   select     Kc: entries per token in idx, with G * Kc <= 49,152 (a group's
+ *              rows are merged in shared memory)
+ *   idx        int32 [tokens, Kc]: each row's positions in [0, S), strictly
+ *              ascending, then -1 for unused entries (the rows dsa_row_topk
+ *              and dsa_combine_window write qualify)
  *   q          bf16 [tokens, heads, 128];  k, v  bf16 [keys, 128]
  *   o          f32 [tokens, heads, 128];  lse  f32 [tokens, heads]
  *   workspace  device memory, 16-byte aligned, of at least

@@ -9,14 +9,14 @@
 // tokens that selected each) and the attention over it.
 //
 // Design (this file's own):
-//   * union: one CTA per group marks the group's positions in a shared-memory
-//     bitmap of the key range, turns per-1024-key chunk popcounts into ranks,
-//     writes the positions in order and ORs each token's bit into the mask of
-//     its positions;
+//   * union: one CTA per group stages the group's rows in shared memory and
+//     merges them, each thread a slice of the key range (no atomics);
 //   * attention: one CTA per group of 128 query/head rows, walking the union
-//     in tiles of 128 positions: four loader warps gather the tile's key rows
-//     into the 128B-swizzled K-major layout the tensor cores read (cp.async)
-//     and write the value rows transposed (8 x 8 transposes in registers);
+//     in tiles of 128 positions: two warps gather the tile's key rows into the
+//     128B-swizzled K-major layout the tensor cores read (cp.async), four write
+//     the value rows transposed (8 x 8 transposes in registers) and one the
+//     tile's token masks, each with its own double-buffered barriers, so a
+//     score tile never waits for value loads;
 //     one thread issues tcgen05.mma (bf16, fp32 accumulators in TMEM) for
 //     S = Q K^T (two TMEM buffers, so the next tile's scores are computed
 //     while this one is normalised) and O += P V; four softmax warps, one
@@ -39,7 +39,8 @@ namespace {
 constexpr int kRows = 128;                 // tokens x heads per group = one MMA tile of rows
 constexpr int kUThreads = 512;
 constexpr int kUWarps = kUThreads / 32;
-constexpr int64_t kMaxAttnKeys = 1 << 20;  // the union bitmap covers at most 2^20 positions (128 KB)
+constexpr int kMaxUG = 16;                 // tokens per group (G = 128 / H, H >= 8)
+constexpr int64_t kMaxUnionRows = 49152;   // G * Kc positions staged in shared memory (192 KB)
 
 __host__ __device__ constexpr int64_t align16(int64_t x) { return (x + 15) & ~(int64_t)15; }
 
@@ -88,75 +89,121 @@ __device__ int block_scan(int v, int* total, int* wtot) {
   return base + x - v;
 }
 
-// Dynamic shared memory: bitmap[nw] u32 | chunk prefix[nchunks] u32.
+__device__ __forceinline__ uint32_t su32_u(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Union of one group's selections by a multi-way merge.  The group's rows
+// (ascending positions, then -1 padding) are staged in shared memory; thread
+// s owns the key range [s S / 512, (s + 1) S / 512), finds where each row
+// enters and leaves it (binary searches), and merges those pieces: every
+// distinct position once, with the bits of the tokens whose piece holds it.
+// A first merge only counts, a block-wide prefix places each thread's output,
+// a second merge writes it -- no atomics, ranks come from the prefix.
+// Dynamic shared memory: rows [G][Kc] int32.
+__device__ __forceinline__ int lower_bound_s(const int32_t* a, int n, int64_t x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)a[mid] < x) lo = mid + 1; else hi = mid;
+  }
+  return lo;
+}
+
 __global__ void __launch_bounds__(kUThreads)
     union_kernel(const int32_t* idx, int32_t T, int32_t Kc, int32_t S, int32_t G, uint8_t* ws, UnionLayout L) {
-  extern __shared__ uint32_t bm[];
+  extern __shared__ int32_t lists[];
   __shared__ int wtot[kUWarps + 1];
+  __shared__ int len[kMaxUG];
   const int grp = blockIdx.x;
   const int t0 = grp * G;
   const int nt = min(G, T - t0);
-  const int nw = (S + 31) >> 5;
-  const int nchunks = (nw + 31) >> 5;
-  uint32_t* cpre = bm + nw;
   uint8_t* rec = ws + (int64_t)grp * L.bytes;
   int32_t* keys = reinterpret_cast<int32_t*>(rec + L.keys_off);
   uint32_t* masks = reinterpret_cast<uint32_t*>(rec + L.masks_off);
   const int32_t* rows = idx + (int64_t)t0 * Kc;
-  const int64_t ne = (int64_t)nt * Kc;
+  const int64_t cap = (int64_t)G * Kc;
 
-  for (int i = threadIdx.x; i < nw; i += kUThreads) bm[i] = 0;
+  if (threadIdx.x < kMaxUG) len[threadIdx.x] = 0;
   __syncthreads();
-  for (int64_t e = threadIdx.x; e < ne; e += kUThreads) {
-    const int32_t j = rows[e];
-    if (j >= 0 && j < S) atomicOr(&bm[j >> 5], 1u << (j & 31));
+  // stage the rows (every copy of a thread in flight at once); a row's length
+  // is the index after its last position
+  for (int g = 0; g < nt; ++g)
+    for (int i = threadIdx.x; i < Kc; i += kUThreads)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32_u(lists + (int64_t)g * Kc + i)),
+                   "l"(rows + (int64_t)g * Kc + i)
+                   : "memory");
+  asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
+  __syncthreads();
+  for (int g = 0; g < nt; ++g) {
+    const int32_t* row = lists + (int64_t)g * Kc;
+    for (int i = threadIdx.x; i < Kc; i += kUThreads)
+      if (row[i] >= 0 && (i + 1 == Kc || row[i + 1] < 0)) len[g] = i + 1;
   }
   __syncthreads();
-  // per-chunk counts, two chunks per thread (nchunks <= 1024), then their prefix
-  int cnt[2] = {0, 0};
+  const int64_t lo = (int64_t)S * threadIdx.x / kUThreads;
+  const int64_t hi = (int64_t)S * (threadIdx.x + 1) / kUThreads;
+  int ptr[kMaxUG], end[kMaxUG];
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int c = 2 * threadIdx.x + u;
-    if (c < nchunks)
-      for (int w = 32 * c; w < min(32 * c + 32, nw); ++w) cnt[u] += __popc(bm[w]);
+  for (int g = 0; g < kMaxUG; ++g) {
+    ptr[g] = end[g] = 0;
+    if (g < nt) {
+      const int32_t* a = lists + (int64_t)g * Kc;
+      ptr[g] = lower_bound_s(a, len[g], lo);
+      end[g] = lower_bound_s(a, len[g], hi);
+    }
   }
-  int total = 0;
-  const int pre = block_scan(cnt[0] + cnt[1], &total, wtot);
-  if (2 * threadIdx.x < nchunks) cpre[2 * threadIdx.x] = pre;
-  if (2 * threadIdx.x + 1 < nchunks) cpre[2 * threadIdx.x + 1] = pre + cnt[0];
-  if (threadIdx.x == 0) *reinterpret_cast<int32_t*>(rec) = total;
-  __syncthreads();
-  // the union in ascending order, and cleared masks
-  for (int c = threadIdx.x; c < nchunks; c += kUThreads) {
-    int pos = (int)cpre[c];
-    for (int w = 32 * c; w < min(32 * c + 32, nw); ++w) {
-      uint32_t x = bm[w];
-      while (x) {
-        const int b = __ffs(x) - 1;
-        x &= x - 1;
-        keys[pos] = (w << 5) + b;
-        masks[pos] = 0u;
-        ++pos;
+  // merge: count, place, merge again and write
+  int count = 0;
+  for (int pass = 0; pass < 2; ++pass) {
+    int q[kMaxUG];
+#pragma unroll
+    for (int g = 0; g < kMaxUG; ++g) q[g] = ptr[g];
+    int out = 0;
+    if (pass == 1) {
+      int total = 0;
+      out = block_scan(count, &total, wtot);
+      // rows that break the contract (unsorted, -1 inside) cannot push the
+      // union past the record or make it name a key outside [0, S)
+      if (threadIdx.x == 0) *reinterpret_cast<int32_t*>(rec) = (int32_t)min((int64_t)total, cap);
+    }
+    while (true) {
+      int32_t key = INT32_MAX;
+#pragma unroll
+      for (int g = 0; g < kMaxUG; ++g)
+        if (q[g] < end[g]) key = min(key, lists[(int64_t)g * Kc + q[g]]);
+      if (key == INT32_MAX) break;
+      uint32_t m = 0;
+#pragma unroll
+      for (int g = 0; g < kMaxUG; ++g)
+        if (q[g] < end[g] && lists[(int64_t)g * Kc + q[g]] == key) {
+          m |= 1u << g;
+          ++q[g];
+        }
+      if (key < 0 || key >= S) continue;
+      if (pass == 0) {
+        ++count;
+      } else {
+        if (out < cap) {
+          keys[out] = key;
+          masks[out] = m;
+        }
+        ++out;
       }
     }
   }
-  __syncthreads();
-  // each selected position's rank in the union gets its token's bit
-  for (int64_t e = threadIdx.x; e < ne; e += kUThreads) {
-    const int32_t j = rows[e];
-    if (j < 0 || j >= S) continue;
-    const int w = j >> 5;
-    int pos = (int)cpre[w >> 5];
-    for (int x = w & ~31; x < w; ++x) pos += __popc(bm[x]);
-    pos += __popc(bm[w] & ((1u << (j & 31)) - 1u));
-    atomicOr(&masks[pos], 1u << (int)(e / Kc));
-  }
 }
 
+// Shapes this build supports; DSA_OK when the call can run.
 // ---------------------------------------------------------------------------
 // attention
 
-constexpr int kAThreads = 384;         // warps 0-3 loaders, 4 MMA, 5-7 idle, 8-11 softmax
+constexpr int kAThreads = 384;  // warps 0-1 K loaders, 2-3 and 6-7 V loaders, 4 MMA, 5 masks, 8-11 softmax
+// Register split (setmaxnreg): 168 per thread at launch (three warps per SM
+// sub-partition); the first two warpgroups drop to 104 so that the softmax
+// warpgroup can keep a whole 128-score row in registers with 240.
+// 256 x 104 + 128 x 240 = 57,344 <= 384 x 168 = 64,512.
+constexpr int kLoadRegs = 104;
+constexpr int kSoftRegs = 240;
+static_assert(256 * kLoadRegs + 128 * kSoftRegs <= kAThreads * 168, "register split exceeds the launch allocation");
 constexpr int kTileN = 128;            // union positions per tile
 constexpr int kDim = 128;              // head_dim = value_dim
 constexpr int kBlk = 128 * 128;        // one 128-row x 128-byte swizzled block
@@ -167,7 +214,7 @@ constexpr int kOffP = kOffV + 4 * kBlk;            // P: 2 blocks (keys 0-63, 64
 constexpr int kOffMask = kOffP + 2 * kBlk;         // per stage, per token: 4 words (128 positions)
 constexpr int kMaxG = 16;
 constexpr int kOffBarA = kOffMask + 2 * kMaxG * 4 * 4;
-constexpr int kNumBarsA = 11;
+constexpr int kNumBarsA = 19;
 constexpr int kOffTmemA = kOffBarA + kNumBarsA * 8;
 constexpr int kSmemA = kOffTmemA + 16 + 1024;       // + slack for the 1024-byte alignment
 constexpr uint32_t kTmemColsA = 512;               // S buffers at 0 and 128, O at 256
@@ -305,8 +352,19 @@ __device__ __forceinline__ void tst32(uint32_t addr, const uint32_t (&r)[32]) {
 __device__ __forceinline__ void tld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ uint16_t to_bf16(float x) {
-  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+// 2^x by the hardware's base-2 exponential (ex2.approx: relative error near
+// 2^-22, far below the bf16 rounding the weights then go through).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// lo and hi rounded to bf16 (nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParams p) {
@@ -316,12 +374,16 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   uint32_t* maskrow = reinterpret_cast<uint32_t*>(base + kOffMask);  // [stage][token][4]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kOffBarA);
   uint64_t* qfull = bars;
-  uint64_t* kvfull = bars + 1;   // [2]
-  uint64_t* kvempty = bars + 3;  // [2]
-  uint64_t* sfull = bars + 5;    // [2]
-  uint64_t* sfree = bars + 7;    // [2]
-  uint64_t* pfull = bars + 9;
-  uint64_t* pvdone = bars + 10;
+  uint64_t* kfull = bars + 1;    // [2] K tile loaded (K loaders)
+  uint64_t* kempty = bars + 3;   // [2] S of that tile done (MMA commit)
+  uint64_t* vfull = bars + 5;    // [2] V^T tile written (V loaders)
+  uint64_t* vempty = bars + 7;   // [2] P V of that tile done (MMA commit)
+  uint64_t* mfull = bars + 9;    // [2] token masks written (mask warp)
+  uint64_t* mempty = bars + 11;  // [2] masks read (softmax)
+  uint64_t* sfull = bars + 13;   // [2] S in TMEM (MMA commit)
+  uint64_t* sfree = bars + 15;   // [2] S read (softmax)
+  uint64_t* pfull = bars + 17;   // P written (softmax)
+  uint64_t* pvdone = bars + 18;  // P V done (MMA commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + kOffTmemA);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -336,10 +398,14 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
 
   if (threadIdx.x == 0) {
     s_attn_abort = 0;
-    bar_init(qfull, 128);
+    bar_init(qfull, 64);
     for (int i = 0; i < 2; ++i) {
-      bar_init(&kvfull[i], 128);
-      bar_init(&kvempty[i], 1);
+      bar_init(&kfull[i], 64);
+      bar_init(&kempty[i], 1);
+      bar_init(&vfull[i], 128);
+      bar_init(&vempty[i], 1);
+      bar_init(&mfull[i], 32);
+      bar_init(&mempty[i], 128);
       bar_init(&sfull[i], 1);
       bar_init(&sfree[i], 128);
     }
@@ -357,110 +423,158 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp < 4) {
-    // ---- loaders: thread tid owns row tid of Q and of each K tile
-    const int tid = threadIdx.x;
-    {
-      const int64_t qr = (int64_t)t0 * p.H + tid;  // query/head row
-      const uint32_t dst = sb + kOffQ;
-      if (qr < (int64_t)p.T * p.H) {
-        const uint16_t* src = p.q + qr * kDim;
-        for (int c = 0; c < 16; ++c) cp16(dst + sw_off(tid, c), src + 8 * c);
-      } else {
-        for (int c = 0; c < 16; ++c) st16(dst + sw_off(tid, c), make_uint4(0, 0, 0, 0));
+  if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLoadRegs));
+    if (warp < 2) {
+      // ---- K loaders: thread tid owns rows 2 tid and 2 tid + 1 of Q and of each K tile
+      const int tid = threadIdx.x;
+      for (int u = 0; u < 2; ++u) {
+        const int row = 2 * tid + u;
+        const int64_t qr = (int64_t)t0 * p.H + row;  // query/head row
+        const uint32_t dst = sb + kOffQ;
+        if (qr < (int64_t)p.T * p.H) {
+          const uint16_t* src = p.q + qr * kDim;
+          for (int c = 0; c < 16; ++c) cp16(dst + sw_off(row, c), src + 8 * c);
+        } else {
+          for (int c = 0; c < 16; ++c) st16(dst + sw_off(row, c), make_uint4(0, 0, 0, 0));
+        }
       }
       cp_wait_all();
       fence_async_smem();
       bar_arrive(qfull);
-    }
-    const int kb = tid & 15;          // V: 8 positions 8 kb .. 8 kb + 7
-    const int db0 = (tid >> 4) * 2;   // V: dims 8 db0 .. 8 db0 + 15
-    for (int i = 0; i < ntiles; ++i) {
-      const int st = i & 1;
-      if (i >= 2 && !bar_wait(&kvempty[st], ((i >> 1) & 1) ^ 1)) break;
-      const int e0 = i * kTileN;
-      // K row tid (zeros past the union)
-      {
-        const int e = e0 + tid;
+      int32_t ck[2], nk[2];
+  #pragma unroll
+      for (int u = 0; u < 2; ++u) ck[u] = 2 * tid + u < n ? ukeys[2 * tid + u] : -1;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !bar_wait(&kempty[st], ((i >> 1) & 1) ^ 1)) break;
         const uint32_t dst = sb + kOffK + st * 2 * kBlk;
-        if (e < n) {
-          const uint16_t* src = p.k + (int64_t)ukeys[e] * kDim;
-          for (int c = 0; c < 16; ++c) cp16(dst + sw_off(tid, c), src + 8 * c);
-        } else {
-          for (int c = 0; c < 16; ++c) st16(dst + sw_off(tid, c), make_uint4(0, 0, 0, 0));
+  #pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int row = 2 * tid + u;
+          if (ck[u] >= 0) {
+            const uint16_t* src = p.k + (int64_t)ck[u] * kDim;
+            for (int c = 0; c < 16; ++c) cp16(dst + sw_off(row, c), src + 8 * c);
+          } else {
+            for (int c = 0; c < 16; ++c) st16(dst + sw_off(row, c), make_uint4(0, 0, 0, 0));
+          }
         }
+        // the next tile's keys while this one's rows are in flight
+  #pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int e = (i + 1) * kTileN + 2 * tid + u;
+          nk[u] = e < n ? ukeys[e] : -1;
+        }
+        cp_wait_all();
+        fence_async_smem();
+        bar_arrive(&kfull[st]);
+        ck[0] = nk[0];
+        ck[1] = nk[1];
       }
-      // V^T: row d holds dim d of the tile's 128 positions
-      {
-        int64_t key[8];
+    } else if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
+      // ---- V loaders (warps 2, 3, 6, 7): thread v owns two 8 x 8 blocks (8
+      // positions x 8 dims) of each tile and writes them transposed: row d of
+      // V^T holds dim d
+      const int v = (warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192 + 64);
+      const int kb = v & 15;           // positions 8 kb .. 8 kb + 7
+      const int db0 = (v >> 4) * 2;    // dims 8 db0 .. 8 db0 + 15
+      int32_t ck[8], nk[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) ck[kk] = 8 * kb + kk < n ? ukeys[8 * kb + kk] : -1;
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i & 1;
+        if (i >= 2 && !bar_wait(&vempty[st], ((i >> 1) & 1) ^ 1)) break;
+        uint4 xx[2][8];  // both blocks in flight before either is transposed
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            xx[u][kk] = ck[kk] >= 0
+                            ? __ldg(reinterpret_cast<const uint4*>(p.v + (int64_t)ck[kk] * kDim + 8 * (db0 + u)))
+                            : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const int e = e0 + 8 * kb + kk;
-          key[kk] = e < n ? (int64_t)ukeys[e] : -1;
+          const int e = (i + 1) * kTileN + 8 * kb + kk;
+          nk[kk] = e < n ? ukeys[e] : -1;
         }
         const uint32_t vbase = sb + kOffV + st * 2 * kBlk;
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
           const int db = db0 + u;
-          uint4 x[8];
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            x[kk] = key[kk] >= 0 ? __ldg(reinterpret_cast<const uint4*>(p.v + key[kk] * kDim + 8 * db))
-                                 : make_uint4(0, 0, 0, 0);
+          const uint4 (&x)[8] = xx[u];
           // 8 x 8 transpose of 16-bit elements: out[dd] = dim dd of the 8 positions
 #pragma unroll
           for (int dd = 0; dd < 8; ++dd) {
             uint32_t w[4];
 #pragma unroll
             for (int pr = 0; pr < 4; ++pr) {
-              const uint32_t* a = reinterpret_cast<const uint32_t*>(&x[2 * pr]);
-              const uint32_t* b = reinterpret_cast<const uint32_t*>(&x[2 * pr + 1]);
-              const uint32_t lo = (a[dd >> 1] >> ((dd & 1) * 16)) & 0xFFFFu;
-              const uint32_t hi = (b[dd >> 1] >> ((dd & 1) * 16)) & 0xFFFFu;
+              const uint32_t* a0 = reinterpret_cast<const uint32_t*>(&x[2 * pr]);
+              const uint32_t* a1 = reinterpret_cast<const uint32_t*>(&x[2 * pr + 1]);
+              const uint32_t lo = (a0[dd >> 1] >> ((dd & 1) * 16)) & 0xFFFFu;
+              const uint32_t hi = (a1[dd >> 1] >> ((dd & 1) * 16)) & 0xFFFFu;
               w[pr] = lo | (hi << 16);
             }
             const int row = 8 * db + dd;
             st16(vbase + sw_off(row, kb), make_uint4(w[0], w[1], w[2], w[3]));
           }
         }
+        fence_async_smem();
+        bar_arrive(&vfull[st]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) ck[kk] = nk[kk];
       }
-      // selection masks of the tile, transposed to one 128-bit row per token
-      {
-        const int e = e0 + 32 * warp + lane;
-        const uint32_t m = e < n ? umasks[e] : 0u;
-        for (int g = 0; g < G; ++g) {
-          const uint32_t b = __ballot_sync(0xFFFFFFFFu, (m >> g) & 1u);
-          if (lane == 0) maskrow[(st * kMaxG + g) * 4 + warp] = b;
-        }
-      }
-      cp_wait_all();
-      fence_async_smem();
-      bar_arrive(&kvfull[st]);
-    }
-  } else if (warp == 4) {
-    // ---- MMA issuer
-    if (lane == 0 && ntiles > 0 && bar_wait(qfull, 0)) {
-      bool ok = true;
-      auto pv = [&](int j) {
-        if (!bar_wait(pfull, j & 1)) return false;
-        fence_after();
-        mma_128(tmem + 256, sb + kOffP, sb + kOffV + (j & 1) * 2 * kBlk, j > 0);
-        mma_commit(pvdone);
-        mma_commit(&kvempty[j & 1]);
-        return true;
-      };
-      for (int i = 0; i < ntiles && ok; ++i) {
+    } else if (warp == 5) {
+      // ---- mask warp: the tile's token masks, one 128-bit row per token;
+      // the next tile's masks are read while this one's are written
+      uint32_t cm[4], nm[4];
+#pragma unroll
+      for (int w = 0; w < 4; ++w) cm[w] = 32 * w + lane < n ? umasks[32 * w + lane] : 0u;
+      for (int i = 0; i < ntiles; ++i) {
         const int st = i & 1;
-        if (!bar_wait(&kvfull[st], (i >> 1) & 1)) break;
-        if (i >= 2 && !bar_wait(&sfree[st], ((i >> 1) & 1) ^ 1)) break;
-        fence_after();
-        mma_128(tmem + st * 128, sb + kOffQ, sb + kOffK + st * 2 * kBlk, false);
-        mma_commit(&sfull[st]);
-        if (i >= 1) ok = pv(i - 1);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int e = (i + 1) * kTileN + 32 * w + lane;
+          nm[w] = e < n ? umasks[e] : 0u;
+        }
+        if (i >= 2 && !bar_wait(&mempty[st], ((i >> 1) & 1) ^ 1)) break;
+#pragma unroll
+        for (int w = 0; w < 4; ++w)
+          for (int g = 0; g < G; ++g) {
+            const uint32_t bit = __ballot_sync(0xFFFFFFFFu, (cm[w] >> g) & 1u);
+            if (lane == 0) maskrow[(st * kMaxG + g) * 4 + w] = bit;
+          }
+        bar_arrive(&mfull[st]);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) cm[w] = nm[w];
       }
-      if (ok) pv(ntiles - 1);
+    } else if (warp == 4) {
+      // ---- MMA issuer
+      if (lane == 0 && ntiles > 0 && bar_wait(qfull, 0)) {
+        bool ok = true;
+        auto pv = [&](int j) {
+          if (!bar_wait(&vfull[j & 1], (j >> 1) & 1)) return false;
+          if (!bar_wait(pfull, j & 1)) return false;
+          fence_after();
+          mma_128(tmem + 256, sb + kOffP, sb + kOffV + (j & 1) * 2 * kBlk, j > 0);
+          mma_commit(pvdone);
+          mma_commit(&vempty[j & 1]);
+          return true;
+        };
+        for (int i = 0; i < ntiles && ok; ++i) {
+          const int st = i & 1;
+          if (!bar_wait(&kfull[st], (i >> 1) & 1)) break;
+          if (i >= 2 && !bar_wait(&sfree[st], ((i >> 1) & 1) ^ 1)) break;
+          fence_after();
+          mma_128(tmem + st * 128, sb + kOffQ, sb + kOffK + st * 2 * kBlk, false);
+          mma_commit(&sfull[st]);
+          mma_commit(&kempty[st]);
+          if (i >= 1) ok = pv(i - 1);
+        }
+        if (ok) pv(ntiles - 1);
+      }
     }
-  } else if (warp >= 8) {
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
     // ---- softmax: thread = query/head row r (TMEM lane)
     const int r = (warp - 8) * 32 + lane;
     const int g = r >> p.log2H, h = r & (p.H - 1);
@@ -480,22 +594,39 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       fence_before();
       bar_arrive(&sfree[st]);
       uint32_t mw[4];
+      __all_sync(0xFFFFFFFFu, bar_wait(&mfull[st], (i >> 1) & 1));
 #pragma unroll
       for (int c = 0; c < 4; ++c) mw[c] = maskrow[(st * kMaxG + g) * 4 + c];
-      float tmax = -INFINITY;
+      bar_arrive(&mempty[st]);
+      // masked, scaled scores (base 2), kept in place, and their maximum
+      // (four partial maxima keep the dependency chains short)
+      float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if ((mw[c] >> j) & 1u) tmax = fmaxf(tmax, __uint_as_float(sc[c][j]) * p.scale_log2);
-      const float m_new = fmaxf(m_used, tmax);
+        for (int j = 0; j < 32; ++j) {
+          const float sv = (mw[c] & (1u << j)) ? __uint_as_float(sc[c][j]) * p.scale_log2 : -INFINITY;
+          sc[c][j] = __float_as_uint(sv);
+          tm[j & 3] = fmaxf(tm[j & 3], sv);
+        }
+      const float m_new = fmaxf(m_used, fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])));
       // the previous tile's P V is done: P may be rewritten, O rescaled
       if (i >= 1) {
         __all_sync(0xFFFFFFFFu, bar_wait(pvdone, (i - 1) & 1));
         fence_after();
       }
+      // The running maximum used for the weights moves only when the row's
+      // maximum rises by more than 8 (a factor 256): until then the weights
+      // exp2(s - m_used) stay below 256, and the final normalisation by the
+      // same m_used makes the result exact, so O is rescaled rarely.
       float alpha = 1.f;
-      if (m_new > m_used && m_used > -INFINITY) alpha = exp2f(m_used - m_new);
+      float m_next = m_used;
+      if (m_used == -INFINITY) {
+        m_next = m_new;  // nothing accumulated yet: O and l are zero
+      } else if (m_new > m_used + 8.f) {
+        m_next = m_new;
+        alpha = ex2(m_used - m_new);
+      }
       if (__any_sync(0xFFFFFFFFu, alpha != 1.f) && i >= 1) {
         // rescale this row of O (warp-wide TMEM access; rows without a change use 1)
 #pragma unroll
@@ -510,9 +641,12 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
         tst_wait();
       }
       l *= alpha;
-      m_used = m_new;
-      // P row (bf16) into the swizzled A tile of the second MMA
+      m_used = m_next;
+      // P row (bf16) into the swizzled A tile of the second MMA: 2^(s - m),
+      // zero for masked positions (2^-inf); a row with nothing selected yet
+      // writes zeros
       const bool any = m_used > -INFINITY;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
 #pragma unroll
@@ -520,20 +654,16 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
           uint32_t w[4];
 #pragma unroll
           for (int pr = 0; pr < 4; ++pr) {
-            float pv2[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              const int j = 8 * q8 + 2 * pr + u;
-              float pj = 0.f;
-              if (any && ((mw[c] >> j) & 1u)) pj = exp2f(__uint_as_float(sc[c][j]) * p.scale_log2 - m_used);
-              l += pj;
-              pv2[u] = pj;
-            }
-            w[pr] = (uint32_t)to_bf16(pv2[0]) | ((uint32_t)to_bf16(pv2[1]) << 16);
+            const int j = 8 * q8 + 2 * pr;
+            const float p0 = any ? ex2(__uint_as_float(sc[c][j]) - m_used) : 0.f;
+            const float p1 = any ? ex2(__uint_as_float(sc[c][j + 1]) - m_used) : 0.f;
+            ls[pr] += p0 + p1;
+            w[pr] = pack_bf16x2(p0, p1);
           }
           st16(sb + kOffP + sw_off(r, 4 * c + q8), make_uint4(w[0], w[1], w[2], w[3]));
         }
       }
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       fence_async_smem();
       fence_before();
       bar_arrive(pfull);
@@ -582,14 +712,11 @@ int check_attention_cfg(const dsa_attention_cfg* c) {
   if (c->tokens < 0 || c->keys < 0 || c->select < 0) return DSA_ERR_INVALID_ARG;
   if (c->heads != 8 && c->heads != 16) return DSA_ERR_UNSUPPORTED;
   if (c->head_dim != 128 || c->value_dim != 128) return DSA_ERR_UNSUPPORTED;
-  if (c->keys > kMaxAttnKeys) return DSA_ERR_UNSUPPORTED;
+  if ((int64_t)(kRows / c->heads) * c->select > kMaxUnionRows) return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
 }
 
-int union_smem(int32_t S) {
-  const int nw = (S + 31) >> 5;
-  return (nw + ((nw + 31) >> 5)) * 4;
-}
+int union_smem(int G, int32_t Kc) { return (int)((int64_t)G * Kc * 4); }
 
 }  // namespace
 
@@ -615,15 +742,15 @@ int dsa_group_union(const dsa_attention_cfg* cfg, const int32_t* idx, void* work
   if (!idx || !workspace || (((uintptr_t)workspace) & 15u) || workspace_bytes < need) return DSA_ERR_INVALID_ARG;
   const int G = kRows / cfg->heads;
   const int groups = (cfg->tokens + G - 1) / G;
-  const int smem = union_smem(cfg->keys);
-  static int configured = 0;
-  if (smem > 48 * 1024 && configured < smem) {
+  const int smem = union_smem(G, cfg->select);
+  static bool configured = false;
+  if (!configured) {
     if (cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             union_smem((int32_t)kMaxAttnKeys)) != cudaSuccess) {
+                             (int)(kMaxUnionRows * 4)) != cudaSuccess) {
       cudaGetLastError();
       return DSA_ERR_CUDA;
     }
-    configured = union_smem((int32_t)kMaxAttnKeys);
+    configured = true;
   }
   union_kernel<<<groups, kUThreads, smem, (cudaStream_t)stream>>>(idx, cfg->tokens, cfg->select, cfg->keys, G,
                                                                    static_cast<uint8_t*>(workspace),

@@ -153,7 +153,7 @@ def test_attention_shapes_checked_without_cuda(lib):
     rc, n = ws(heads=16)
     assert rc == dsa.DSA_OK and n == 5 * (16 + 2 * 8 * 64 * 4)
     for kw in (dict(heads=4), dict(heads=32), dict(head_dim=64), dict(value_dim=256),
-               dict(keys=(1 << 20) + 1)):
+               dict(select=3073), dict(heads=16, select=6145)):
         assert ws(**kw)[0] == dsa.DSA_ERR_UNSUPPORTED, kw
     for kw in (dict(tokens=-1), dict(select=-2), dict(keys=-5)):
         assert ws(**kw)[0] == dsa.DSA_ERR_INVALID_ARG, kw

@@ -110,23 +110,28 @@ def test_edge_selections():
         idx[3] = -1                       # nothing selected
         idx[4] = -1
         idx[4, 0] = 17                    # one position
-        idx[5, ::2] = -1                  # holes inside the row
+        idx[5, 20:] = -1                  # a shorter row
         idx[20] = -1
-        idx[20, :3] = [0, 4999, 2500]     # first and last key, unsorted
+        idx[20, :3] = [0, 2500, 4999]     # first and last key
         return idx
     _run(33, 8, 5000, 48, seed=4, idx_fn=f)
 
 
 def test_full_key_range_and_wide_selection():
-    # keys at the 2^20 limit and 2048-entry selections (the row top-k's size)
+    # 2^20 keys and 2048-entry selections (the row top-k's size)
     _run(32, 8, 1 << 20, 2048, seed=5, own=0.05)
+
+
+def test_widest_group_rows():
+    # G * Kc at its limit: 8 tokens x 6144 positions (16 heads)
+    _run(16, 16, 1 << 18, 6144, seed=6, own=0.3)
 
 
 def test_unsupported_shapes():
     torch = _torch()
     import sparse_attention_indexer_live_gb300 as dsa
     n = torch.empty(1)
-    for kw in (dict(heads=4), dict(head_dim=64), dict(keys=(1 << 20) + 1)):
+    for kw in (dict(heads=4), dict(head_dim=64), dict(select=3073)):
         c = dict(tokens=8, heads=8, keys=1000, head_dim=128, value_dim=128, select=16)
         c.update(kw)
         with pytest.raises(dsa.DsaSelectError) as e:

@@ -331,8 +331,10 @@ def attention_inputs(T: int, H: int, S: int, Kc: int, seed: int = 9, dim: int = 
     idx = np.full((T, Kc), -1, dtype=np.int32)
     n = max(0, min(int(round(fill * Kc)), S))
     for g0 in range(0, T, G):
-        base = u32(seed, _S_ASEL, g0, 4 * Kc + 64) % max(S, 1)
-        base = np.unique(base)[:n] if n else base[:0]
+        base = np.unique(u32(seed, _S_ASEL, g0, 4 * Kc + 64) % max(S, 1))
+        # n of the distinct draws, spread over their whole range
+        base = base[np.linspace(0, len(base) - 1, n).astype(np.int64)] if n else base[:0]
+        base = np.unique(base)
         for t in range(g0, min(g0 + G, T)):
             r = u32(seed, _S_ATOK, t, 2 * Kc + 8)
             sel = base.copy()
