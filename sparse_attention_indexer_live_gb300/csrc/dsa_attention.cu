@@ -40,7 +40,7 @@ constexpr int kRows = 128;                 // tokens x heads per group = one MMA
 constexpr int kUThreads = 512;
 constexpr int kUWarps = kUThreads / 32;
 constexpr int kMaxUG = 16;                 // tokens per group (G = 128 / H, H >= 8)
-constexpr int64_t kMaxUnionRows = 49152;   // G * Kc positions staged in shared memory (192 KB)
+constexpr int64_t kMaxUnionRows = 49152;   // G * Kc positions staged in shared memory (192 KB + 16 KB starts)
 
 __host__ __device__ constexpr int64_t align16(int64_t x) { return (x + 15) & ~(int64_t)15; }
 
@@ -92,103 +92,173 @@ __device__ int block_scan(int v, int* total, int* wtot) {
 __device__ __forceinline__ uint32_t su32_u(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
 // Union of one group's selections by a multi-way merge.  The group's rows
-// (ascending positions, then -1 padding) are staged in shared memory; thread
-// s owns the key range [s S / 512, (s + 1) S / 512), finds where each row
-// enters and leaves it (binary searches), and merges those pieces: every
-// distinct position once, with the bits of the tokens whose piece holds it.
-// A first merge only counts, a block-wide prefix places each thread's output,
-// a second merge writes it -- no atomics, ranks come from the prefix.
-// Dynamic shared memory: rows [G][Kc] int32.
-__device__ __forceinline__ int lower_bound_s(const int32_t* a, int n, int64_t x) {
-  int lo = 0, hi = n;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if ((int64_t)a[mid] < x) lo = mid + 1; else hi = mid;
-  }
-  return lo;
+// (ascending positions, then -1 padding) are staged in shared memory.  Key
+// space is cut into 512 ranges by a shift of the key; thread s owns range s.
+// One coalesced pass over every row records, per row and range, where the
+// row enters the range (a row's entries of range s are [start[s],
+// start[s + 1])).  Each thread then merges its pieces once, holding the
+// current head of every row in a register so that only the rows it advances
+// are read again: every distinct position once, with the bits of the tokens
+// whose rows hold it.  The merged output goes to provisional slots (a prefix
+// of the pieces' sizes, which bound it); a block-wide prefix of the real
+// counts then gives the final ranks and the output is compacted through the
+// shared memory the rows occupied -- no atomics.
+// Dynamic shared memory: rows [G][Kc] int32 | start [G][513] uint16.
+constexpr int kUBuckets = kUThreads;
+
+__device__ __forceinline__ int ubucket(int32_t key, int shift) {
+  return min(max(key, 0) >> shift, kUBuckets - 1);
 }
 
+// head = lists[addr] when p, else unchanged (no branch)
+__device__ __forceinline__ int32_t lds_if(bool p, uint32_t addr, int32_t head) {
+  asm volatile(
+      "{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q ld.shared.b32 %0, [%1];\n}\n"
+      : "+r"(head)
+      : "r"(addr), "r"((uint32_t)p)
+      : "memory");
+  return head;
+}
+
+template <int kG>
 __global__ void __launch_bounds__(kUThreads)
-    union_kernel(const int32_t* idx, int32_t T, int32_t Kc, int32_t S, int32_t G, uint8_t* ws, UnionLayout L) {
-  extern __shared__ int32_t lists[];
+    union_kernel(const int32_t* idx, int32_t T, int32_t Kc, int32_t S, uint8_t* ws, UnionLayout L) {
+  extern __shared__ __align__(16) int32_t lists[];
   __shared__ int wtot[kUWarps + 1];
-  __shared__ int len[kMaxUG];
+  __shared__ int len[kG];
   const int grp = blockIdx.x;
-  const int t0 = grp * G;
-  const int nt = min(G, T - t0);
+  const int t0 = grp * kG;
+  const int nt = min(kG, T - t0);
   uint8_t* rec = ws + (int64_t)grp * L.bytes;
   int32_t* keys = reinterpret_cast<int32_t*>(rec + L.keys_off);
   uint32_t* masks = reinterpret_cast<uint32_t*>(rec + L.masks_off);
   const int32_t* rows = idx + (int64_t)t0 * Kc;
-  const int64_t cap = (int64_t)G * Kc;
+  const int cap = kG * Kc;
+  uint16_t* start = reinterpret_cast<uint16_t*>(lists + cap);
+  // key >> shift < 512 for every key in [0, S)
+  int shift = 0;
+  while (((int64_t)(S - 1) >> shift) >= kUBuckets) ++shift;
 
-  if (threadIdx.x < kMaxUG) len[threadIdx.x] = 0;
-  __syncthreads();
-  // stage the rows (every copy of a thread in flight at once); a row's length
-  // is the index after its last position
-  for (int g = 0; g < nt; ++g)
-    for (int i = threadIdx.x; i < Kc; i += kUThreads)
-      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32_u(lists + (int64_t)g * Kc + i)),
-                   "l"(rows + (int64_t)g * Kc + i)
-                   : "memory");
+  // stage the rows: one contiguous block of nt Kc entries (every copy of a
+  // thread in flight at once)
+  const int total_in = nt * Kc;
+  if ((Kc & 3) == 0 && (reinterpret_cast<uintptr_t>(rows) & 15) == 0) {
+    for (int i = 4 * threadIdx.x; i < total_in; i += 4 * kUThreads)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32_u(lists + i)), "l"(rows + i) : "memory");
+  } else {
+    for (int i = threadIdx.x; i < total_in; i += kUThreads)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32_u(lists + i)), "l"(rows + i) : "memory");
+  }
   asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
   __syncthreads();
-  for (int g = 0; g < nt; ++g) {
-    const int32_t* row = lists + (int64_t)g * Kc;
-    for (int i = threadIdx.x; i < Kc; i += kUThreads)
-      if (row[i] >= 0 && (i + 1 == Kc || row[i + 1] < 0)) len[g] = i + 1;
+  // a row's length: its entries are valid (>= 0) up to the padding
+  if (threadIdx.x < nt) {
+    const int32_t* row = lists + threadIdx.x * Kc;
+    int lo = 0, hi = Kc;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (row[mid] >= 0) lo = mid + 1; else hi = mid;
+    }
+    len[threadIdx.x] = lo;
   }
   __syncthreads();
-  const int64_t lo = (int64_t)S * threadIdx.x / kUThreads;
-  const int64_t hi = (int64_t)S * (threadIdx.x + 1) / kUThreads;
-  int ptr[kMaxUG], end[kMaxUG];
+  // where each row enters each range: entry i writes the ranges between its
+  // predecessor's and its own, so that start[s] = first entry of range >= s.
+  // Neighbouring entries mostly share a range or sit in adjacent ones: one
+  // write, and a loop only across empty ranges.
+#pragma unroll 1
+  for (int g = 0; g < nt; ++g) {
+    const int n = len[g];
+    const int32_t* row = lists + g * Kc;
+    uint16_t* st = start + g * (kUBuckets + 1);
+    for (int i0 = 4 * threadIdx.x; i0 <= n; i0 += 4 * kUThreads) {
+      int b[5];
+      b[0] = i0 == 0 ? -1 : ubucket(row[i0 - 1], shift);
 #pragma unroll
-  for (int g = 0; g < kMaxUG; ++g) {
-    ptr[g] = end[g] = 0;
-    if (g < nt) {
-      const int32_t* a = lists + (int64_t)g * Kc;
-      ptr[g] = lower_bound_s(a, len[g], lo);
-      end[g] = lower_bound_s(a, len[g], hi);
-    }
-  }
-  // merge: count, place, merge again and write
-  int count = 0;
-  for (int pass = 0; pass < 2; ++pass) {
-    int q[kMaxUG];
+      for (int u = 0; u < 4; ++u) b[u + 1] = i0 + u < n ? ubucket(row[i0 + u], shift) : kUBuckets;
 #pragma unroll
-    for (int g = 0; g < kMaxUG; ++g) q[g] = ptr[g];
-    int out = 0;
-    if (pass == 1) {
-      int total = 0;
-      out = block_scan(count, &total, wtot);
-      // rows that break the contract (unsorted, -1 inside) cannot push the
-      // union past the record or make it name a key outside [0, S)
-      if (threadIdx.x == 0) *reinterpret_cast<int32_t*>(rec) = (int32_t)min((int64_t)total, cap);
-    }
-    while (true) {
-      int32_t key = INT32_MAX;
-#pragma unroll
-      for (int g = 0; g < kMaxUG; ++g)
-        if (q[g] < end[g]) key = min(key, lists[(int64_t)g * Kc + q[g]]);
-      if (key == INT32_MAX) break;
-      uint32_t m = 0;
-#pragma unroll
-      for (int g = 0; g < kMaxUG; ++g)
-        if (q[g] < end[g] && lists[(int64_t)g * Kc + q[g]] == key) {
-          m |= 1u << g;
-          ++q[g];
+      for (int u = 0; u < 4; ++u) {
+        const int i = i0 + u;
+        if (i <= n && b[u + 1] > b[u]) {
+          st[b[u] + 1] = (uint16_t)i;
+          for (int x = b[u] + 2; x <= b[u + 1]; ++x) st[x] = (uint16_t)i;
         }
-      if (key < 0 || key >= S) continue;
-      if (pass == 0) {
-        ++count;
-      } else {
-        if (out < cap) {
-          keys[out] = key;
-          masks[out] = m;
-        }
-        ++out;
       }
     }
+  }
+  __syncthreads();
+  // this thread's piece of each row; the clamps keep rows that break the
+  // contract (unsorted) inside the row
+  int q[kG], end[kG];
+  int pieces = 0;
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    q[g] = end[g] = 0;
+    if (g < nt) {
+      const uint16_t* st = start + g * (kUBuckets + 1);
+      q[g] = min((int)st[threadIdx.x], len[g]);
+      end[g] = max(q[g], min((int)st[threadIdx.x + 1], len[g]));
+      pieces += end[g] - q[g];
+    }
+  }
+  int total = 0;
+  const int prov = block_scan(pieces, &total, wtot);
+  // merge into the provisional slots [prov, prov + pieces)
+  int32_t head[kG];
+  uint32_t addr[kG];
+#pragma unroll
+  for (int g = 0; g < kG; ++g) {
+    addr[g] = su32_u(lists + g * Kc + q[g]);
+    head[g] = lds_if(q[g] < end[g], addr[g], INT32_MAX);
+  }
+  int out = 0;
+  while (true) {
+    int32_t mn[kG];
+#pragma unroll
+    for (int g = 0; g < kG; ++g) mn[g] = head[g];
+#pragma unroll
+    for (int w = kG / 2; w >= 1; w >>= 1)
+#pragma unroll
+      for (int g = 0; g < w; ++g) mn[g] = min(mn[g], mn[g + w]);
+    const int32_t key = mn[0];
+    if (key == INT32_MAX) break;
+    uint32_t m = 0;
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+      const bool hit = head[g] == key;
+      m |= (uint32_t)hit << g;
+      q[g] += hit;
+      addr[g] += hit ? 4u : 0u;
+      const bool more = q[g] < end[g];
+      head[g] = lds_if(hit && more, addr[g], hit && !more ? INT32_MAX : head[g]);
+    }
+    if (key >= 0 && key < S && prov + out < cap) {
+      keys[prov + out] = key;
+      masks[prov + out] = m;
+      ++out;
+    }
+  }
+  // final ranks; rows that break the contract cannot push the union past the
+  // record or make it name a key outside [0, S)
+  int n = 0;
+  const int fin = block_scan(out, &n, wtot);
+  if (threadIdx.x == 0) *reinterpret_cast<int32_t*>(rec) = n;
+  // compact keys, then masks, through the rows' shared memory (the reads of
+  // a thread's provisional slots go out eight at a time)
+  for (int half = 0; half < 2; ++half) {
+    uint32_t* src = half == 0 ? reinterpret_cast<uint32_t*>(keys) : masks;
+    uint32_t* stage = reinterpret_cast<uint32_t*>(lists);
+    __syncthreads();
+    for (int j0 = 0; j0 < out; j0 += 8) {
+      uint32_t x[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) x[u] = j0 + u < out ? src[prov + j0 + u] : 0u;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (j0 + u < out) stage[fin + j0 + u] = x[u];
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += kUThreads) src[i] = stage[i];
   }
 }
 
@@ -716,7 +786,7 @@ int check_attention_cfg(const dsa_attention_cfg* c) {
   return DSA_OK;
 }
 
-int union_smem(int G, int32_t Kc) { return (int)((int64_t)G * Kc * 4); }
+int union_smem(int G, int32_t Kc) { return (int)((int64_t)G * Kc * 4 + G * (kUBuckets + 1) * 2); }
 
 }  // namespace
 
@@ -745,16 +815,18 @@ int dsa_group_union(const dsa_attention_cfg* cfg, const int32_t* idx, void* work
   const int smem = union_smem(G, cfg->select);
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kMaxUnionRows * 4)) != cudaSuccess) {
+    const int most = (int)(kMaxUnionRows * 4 + kMaxUG * (kUBuckets + 1) * 2);
+    if (cudaFuncSetAttribute(union_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) != cudaSuccess ||
+        cudaFuncSetAttribute(union_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) != cudaSuccess) {
       cudaGetLastError();
       return DSA_ERR_CUDA;
     }
     configured = true;
   }
-  union_kernel<<<groups, kUThreads, smem, (cudaStream_t)stream>>>(idx, cfg->tokens, cfg->select, cfg->keys, G,
-                                                                   static_cast<uint8_t*>(workspace),
-                                                                   union_layout(G, cfg->select));
+  auto* kern = G == 8 ? union_kernel<8> : union_kernel<16>;
+  kern<<<groups, kUThreads, smem, (cudaStream_t)stream>>>(idx, cfg->tokens, cfg->select, cfg->keys,
+                                                          static_cast<uint8_t*>(workspace),
+                                                          union_layout(G, cfg->select));
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

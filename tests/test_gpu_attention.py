@@ -117,6 +117,12 @@ def test_edge_selections():
     _run(33, 8, 5000, 48, seed=4, idx_fn=f)
 
 
+def test_selection_width_not_a_multiple_of_four():
+    # rows of 50 and 37 entries: the union stages them four bytes at a time
+    _run(21, 8, 3000, 50, seed=7, own=0.3)
+    _run(13, 16, 2000, 37, seed=8, own=0.3, fill=0.9)
+
+
 def test_full_key_range_and_wide_selection():
     # 2^20 keys and 2048-entry selections (the row top-k's size)
     _run(32, 8, 1 << 20, 2048, seed=5, own=0.05)

@@ -343,8 +343,14 @@ def attention_inputs(T: int, H: int, S: int, Kc: int, seed: int = 9, dim: int = 
                 swap = np.unique(r[:m] % len(sel))
                 sel[swap] = r[Kc:Kc + len(swap)] % S
             sel = np.unique(sel)
-            # refill to n distinct positions if replacements collided
-            extra = r[Kc + m:] % S
-            sel = np.unique(np.concatenate([sel, extra]))[:n] if len(sel) < n else sel[:n]
-            idx[t, :len(sel)] = np.sort(sel)
+            if len(sel) < n:
+                # replacements collided: top up with the token's further draws,
+                # in draw order, then (tiny key ranges) with the lowest free keys
+                extra = r[Kc + m:] % S
+                extra = extra[~np.isin(extra, sel)]
+                _, first = np.unique(extra, return_index=True)
+                sel = np.union1d(sel, extra[np.sort(first)][:n - len(sel)])
+                if len(sel) < n:
+                    sel = np.union1d(sel, np.setdiff1d(np.arange(S), sel)[:n - len(sel)])
+            idx[t, :n] = sel[:n]
     return q, k, v, idx
