@@ -262,28 +262,32 @@ __global__ void __launch_bounds__(kUThreads)
   }
 }
 
-// Shapes this build supports; DSA_OK when the call can run.
 // ---------------------------------------------------------------------------
 // attention
 
-constexpr int kAThreads = 384;  // warps 0-1 K loaders, 2-3 and 6-7 V loaders, 4 MMA, 5 masks, 8-11 softmax
-// Register split (setmaxnreg): 168 per thread at launch (three warps per SM
-// sub-partition); the first two warpgroups drop to 104 so that the softmax
-// warpgroup can keep a whole 128-score row in registers with 240.
-// 256 x 104 + 128 x 240 = 57,344 <= 384 x 168 = 64,512.
-constexpr int kLoadRegs = 104;
-constexpr int kSoftRegs = 240;
-static_assert(256 * kLoadRegs + 128 * kSoftRegs <= kAThreads * 168, "register split exceeds the launch allocation");
+constexpr int kAThreads = 512;  // warps 0-1 Q/K loaders, 2-3 V loaders, 4 MMA, 5 masks, 6-7 idle, 8-15 softmax
+// Register split (setmaxnreg): 128 per thread at launch (the whole register
+// file for 512 threads); the first two warpgroups drop to 88 so that each
+// softmax thread can keep its 64 scores of a row in registers with 168.
+// 256 x 88 + 256 x 168 = 65,536 = 512 x 128.  The host refuses the launch
+// when the compiled kernel asks for fewer than kALaunchRegs (the increase
+// would then wait for registers that never free up).
+constexpr int kLoadRegs = 88;
+constexpr int kSoftRegs = 168;
+constexpr int kALaunchRegs = 128;
+static_assert(256 * kLoadRegs + 256 * kSoftRegs <= kAThreads * kALaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kTileN = 128;            // union positions per tile
 constexpr int kDim = 128;              // head_dim = value_dim
 constexpr int kBlk = 128 * 128;        // one 128-row x 128-byte swizzled block
 constexpr int kOffQ = 0;               // Q: 2 blocks (dims 0-63, 64-127)
 constexpr int kOffK = kOffQ + 2 * kBlk;            // K: 2 stages x 2 blocks
-constexpr int kOffV = kOffK + 4 * kBlk;            // V^T: 2 stages x 2 blocks (keys 0-63, 64-127)
+constexpr int kOffV = kOffK + 4 * kBlk;            // V: 2 stages x 2 blocks (dims 0-63, 64-127), like K
 constexpr int kOffP = kOffV + 4 * kBlk;            // P: 2 blocks (keys 0-63, 64-127)
 constexpr int kOffMask = kOffP + 2 * kBlk;         // per stage, per token: 4 words (128 positions)
 constexpr int kMaxG = 16;
-constexpr int kOffBarA = kOffMask + 2 * kMaxG * 4 * 4;
+constexpr int kOffXch = kOffMask + 2 * kMaxG * 4 * 4;  // [tile parity][half][row] partial row maxima
+constexpr int kOffBarA = kOffXch + 2 * 2 * 128 * 4;
 constexpr int kNumBarsA = 19;
 constexpr int kOffTmemA = kOffBarA + kNumBarsA * 8;
 constexpr int kSmemA = kOffTmemA + 16 + 1024;       // + slack for the 1024-byte alignment
@@ -393,6 +397,39 @@ __device__ __forceinline__ void mma_128(uint32_t d, uint32_t a, uint32_t b, bool
         "l"(ad), "l"(bd), "r"(kIdescA), "r"(en));
   }
 }
+// The value tile as the B operand of O += P V without a transpose: V rows
+// (positions) are the K dimension and dims the N dimension, stored like a K
+// tile (128B-swizzled rows of 64 dims), i.e. N-major.  Leading byte offset:
+// the next 64 dims (second block); stride byte offset: the next 8 positions.
+__device__ __forceinline__ uint64_t sdesc_nmajor(uint32_t a) {
+  uint64_t d = (uint64_t)((a & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(kBlk >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+constexpr uint32_t kIdescPV = kIdescA | (1u << 16);  // B N-major
+
+// O (+)= P V over K = 128 positions (eight K = 16 steps of 16 rows of V).
+__device__ __forceinline__ void mma_pv(uint32_t d, uint32_t a, uint32_t b, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint64_t ad = sdesc(a + (uint32_t)((kk >> 2) * kBlk + (kk & 3) * 32));
+    const uint64_t bd = sdesc_nmajor(b + (uint32_t)(kk * 16 * 128));
+    const uint32_t en = (acc || kk > 0) ? 1u : 0u;
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+        "l"(ad), "l"(bd), "r"(kIdescPV), "r"(en));
+  }
+}
+__device__ __forceinline__ void cp_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void named_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(su32(b))
                : "memory");
@@ -442,11 +479,12 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(araw) + 1023) & ~(uintptr_t)1023);
   const uint32_t sb = su32(base);
   uint32_t* maskrow = reinterpret_cast<uint32_t*>(base + kOffMask);  // [stage][token][4]
+  float* xch = reinterpret_cast<float*>(base + kOffXch);              // [parity][half][row]
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kOffBarA);
   uint64_t* qfull = bars;
   uint64_t* kfull = bars + 1;    // [2] K tile loaded (K loaders)
   uint64_t* kempty = bars + 3;   // [2] S of that tile done (MMA commit)
-  uint64_t* vfull = bars + 5;    // [2] V^T tile written (V loaders)
+  uint64_t* vfull = bars + 5;    // [2] V tile loaded (V loaders)
   uint64_t* vempty = bars + 7;   // [2] P V of that tile done (MMA commit)
   uint64_t* mfull = bars + 9;    // [2] token masks written (mask warp)
   uint64_t* mempty = bars + 11;  // [2] masks read (softmax)
@@ -472,14 +510,14 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
     for (int i = 0; i < 2; ++i) {
       bar_init(&kfull[i], 64);
       bar_init(&kempty[i], 1);
-      bar_init(&vfull[i], 128);
+      bar_init(&vfull[i], 64);
       bar_init(&vempty[i], 1);
       bar_init(&mfull[i], 32);
-      bar_init(&mempty[i], 128);
+      bar_init(&mempty[i], 256);
       bar_init(&sfull[i], 1);
-      bar_init(&sfree[i], 128);
+      bar_init(&sfree[i], 256);
     }
-    bar_init(pfull, 128);
+    bar_init(pfull, 256);
     bar_init(pvdone, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -495,104 +533,64 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
 
   if (warp < 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLoadRegs));
-    if (warp < 2) {
-      // ---- K loaders: thread tid owns rows 2 tid and 2 tid + 1 of Q and of each K tile
-      const int tid = threadIdx.x;
-      for (int u = 0; u < 2; ++u) {
-        const int row = 2 * tid + u;
-        const int64_t qr = (int64_t)t0 * p.H + row;  // query/head row
-        const uint32_t dst = sb + kOffQ;
-        if (qr < (int64_t)p.T * p.H) {
-          const uint16_t* src = p.q + qr * kDim;
-          for (int c = 0; c < 16; ++c) cp16(dst + sw_off(row, c), src + 8 * c);
-        } else {
-          for (int c = 0; c < 16; ++c) st16(dst + sw_off(row, c), make_uint4(0, 0, 0, 0));
-        }
-      }
-      cp_wait_all();
-      fence_async_smem();
-      bar_arrive(qfull);
-      int32_t ck[2], nk[2];
-  #pragma unroll
-      for (int u = 0; u < 2; ++u) ck[u] = 2 * tid + u < n ? ukeys[2 * tid + u] : -1;
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i & 1;
-        if (i >= 2 && !bar_wait(&kempty[st], ((i >> 1) & 1) ^ 1)) break;
-        const uint32_t dst = sb + kOffK + st * 2 * kBlk;
-  #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int row = 2 * tid + u;
-          if (ck[u] >= 0) {
-            const uint16_t* src = p.k + (int64_t)ck[u] * kDim;
-            for (int c = 0; c < 16; ++c) cp16(dst + sw_off(row, c), src + 8 * c);
-          } else {
-            for (int c = 0; c < 16; ++c) st16(dst + sw_off(row, c), make_uint4(0, 0, 0, 0));
-          }
-        }
-        // the next tile's keys while this one's rows are in flight
-  #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int e = (i + 1) * kTileN + 2 * tid + u;
-          nk[u] = e < n ? ukeys[e] : -1;
+    if (warp < 4) {
+      // ---- loaders: warps 0-1 Q and K, warps 2-3 V.  Warp w of a pair owns
+      // rows 64 w .. 64 w + 63 of each tile; one copy instruction moves two
+      // whole rows (a half-warp per 256-byte row, 16 bytes a lane), so every
+      // request is a full row.  Lane l holds the keys of rows 2 l and 2 l + 1
+      // of its warp's share and hands them round by shuffles.  Two tiles stay
+      // in flight: tile i is announced once tile i + 1 has been issued.
+      const bool is_k = warp < 2;
+      const int wrow = 64 * (warp & 1);       // first row of this warp's share
+      const int half = lane >> 4, c = lane & 15;
+      const uint16_t* rows_src = is_k ? p.k : p.v;
+      uint64_t* full = is_k ? kfull : vfull;
+      uint64_t* empty = is_k ? kempty : vempty;
+      const uint32_t tile_base = sb + (is_k ? kOffK : kOffV);
+      if (is_k) {
+        for (int j = 0; j < 32; ++j) {
+          const int row = wrow + 2 * j + half;
+          const int64_t qr = (int64_t)t0 * p.H + row;  // query/head row
+          if (qr < (int64_t)p.T * p.H)
+            cp16(sb + kOffQ + sw_off(row, c), p.q + qr * kDim + 8 * c);
+          else
+            st16(sb + kOffQ + sw_off(row, c), make_uint4(0, 0, 0, 0));
         }
         cp_wait_all();
         fence_async_smem();
-        bar_arrive(&kfull[st]);
-        ck[0] = nk[0];
-        ck[1] = nk[1];
+        bar_arrive(qfull);
       }
-    } else if (warp == 2 || warp == 3 || warp == 6 || warp == 7) {
-      // ---- V loaders (warps 2, 3, 6, 7): thread v owns two 8 x 8 blocks (8
-      // positions x 8 dims) of each tile and writes them transposed: row d of
-      // V^T holds dim d
-      const int v = (warp < 4 ? threadIdx.x - 64 : threadIdx.x - 192 + 64);
-      const int kb = v & 15;           // positions 8 kb .. 8 kb + 7
-      const int db0 = (v >> 4) * 2;    // dims 8 db0 .. 8 db0 + 15
-      int32_t ck[8], nk[8];
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) ck[kk] = 8 * kb + kk < n ? ukeys[8 * kb + kk] : -1;
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i & 1;
-        if (i >= 2 && !bar_wait(&vempty[st], ((i >> 1) & 1) ^ 1)) break;
-        uint4 xx[2][8];  // both blocks in flight before either is transposed
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            xx[u][kk] = ck[kk] >= 0
-                            ? __ldg(reinterpret_cast<const uint4*>(p.v + (int64_t)ck[kk] * kDim + 8 * (db0 + u)))
-                            : make_uint4(0, 0, 0, 0);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const int e = (i + 1) * kTileN + 8 * kb + kk;
-          nk[kk] = e < n ? ukeys[e] : -1;
-        }
-        const uint32_t vbase = sb + kOffV + st * 2 * kBlk;
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int db = db0 + u;
-          const uint4 (&x)[8] = xx[u];
-          // 8 x 8 transpose of 16-bit elements: out[dd] = dim dd of the 8 positions
-#pragma unroll
-          for (int dd = 0; dd < 8; ++dd) {
-            uint32_t w[4];
-#pragma unroll
-            for (int pr = 0; pr < 4; ++pr) {
-              const uint32_t* a0 = reinterpret_cast<const uint32_t*>(&x[2 * pr]);
-              const uint32_t* a1 = reinterpret_cast<const uint32_t*>(&x[2 * pr + 1]);
-              const uint32_t lo = (a0[dd >> 1] >> ((dd & 1) * 16)) & 0xFFFFu;
-              const uint32_t hi = (a1[dd >> 1] >> ((dd & 1) * 16)) & 0xFFFFu;
-              w[pr] = lo | (hi << 16);
-            }
-            const int row = 8 * db + dd;
-            st16(vbase + sw_off(row, kb), make_uint4(w[0], w[1], w[2], w[3]));
+      int32_t ck0 = wrow + 2 * lane < n ? ukeys[wrow + 2 * lane] : -1;
+      int32_t ck1 = wrow + 2 * lane + 1 < n ? ukeys[wrow + 2 * lane + 1] : -1;
+      for (int i = 0; i <= ntiles; ++i) {
+        if (i < ntiles) {
+          const int st = i & 1;
+          if (i >= 2 && !bar_wait(&empty[st], ((i >> 1) & 1) ^ 1)) break;
+          const uint32_t dst = tile_base + st * 2 * kBlk;
+#pragma unroll 8
+          for (int j = 0; j < 32; ++j) {
+            const int32_t k0 = __shfl_sync(0xFFFFFFFFu, ck0, j);
+            const int32_t k1 = __shfl_sync(0xFFFFFFFFu, ck1, j);
+            const int32_t key = half ? k1 : k0;
+            const int row = wrow + 2 * j + half;
+            if (key >= 0)
+              cp16(dst + sw_off(row, c), rows_src + (int64_t)key * kDim + 8 * c);
+            else
+              st16(dst + sw_off(row, c), make_uint4(0, 0, 0, 0));
           }
+          cp_commit();
+          const int e = (i + 1) * kTileN + wrow + 2 * lane;
+          ck0 = e < n ? ukeys[e] : -1;
+          ck1 = e + 1 < n ? ukeys[e + 1] : -1;
         }
-        fence_async_smem();
-        bar_arrive(&vfull[st]);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) ck[kk] = nk[kk];
+        if (i >= 1) {
+          // tile i - 1 has landed (only tile i may still be in flight)
+          if (i < ntiles) cp_wait_1(); else cp_wait_all();
+          fence_async_smem();
+          bar_arrive(&full[(i - 1) & 1]);
+        }
       }
+      cp_wait_all();  // nothing of this thread still in flight (also after an abort)
     } else if (warp == 5) {
       // ---- mask warp: the tile's token masks, one 128-bit row per token;
       // the next tile's masks are read while this one's are written
@@ -625,7 +623,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
           if (!bar_wait(&vfull[j & 1], (j >> 1) & 1)) return false;
           if (!bar_wait(pfull, j & 1)) return false;
           fence_after();
-          mma_128(tmem + 256, sb + kOffP, sb + kOffV + (j & 1) * 2 * kBlk, j > 0);
+          mma_pv(tmem + 256, sb + kOffP, sb + kOffV + (j & 1) * 2 * kBlk, j > 0);
           mma_commit(pvdone);
           mma_commit(&vempty[j & 1]);
           return true;
@@ -645,41 +643,51 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftRegs));
-    // ---- softmax: thread = query/head row r (TMEM lane)
-    const int r = (warp - 8) * 32 + lane;
+    // ---- softmax: two warpgroups; thread = query/head row r (TMEM lane) and
+    // one half of the tile's columns (64 positions; O columns: 64 dims)
+    const int sw = warp - 8;
+    const int hf = sw >> 2;
+    const int r = (sw & 3) * 32 + lane;
     const int g = r >> p.log2H, h = r & (p.H - 1);
     const int t = t0 + g;
-    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const int pair_bar = 1 + (sw & 3);  // named barrier of the two warps sharing these rows
+    const uint32_t lane_base = tmem + ((uint32_t)((sw & 3) * 32) << 16);
     float m_used = -INFINITY, l = 0.f;
     for (int i = 0; i < ntiles; ++i) {
       const int st = i & 1;
       const bool okw = __all_sync(0xFFFFFFFFu, bar_wait(&sfull[st], (i >> 1) & 1));
       fence_after();
-      uint32_t sc[4][32];
+      uint32_t sc[2][32];
       if (okw) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) tld32(lane_base + st * 128 + 32 * c, sc[c]);
+        for (int c = 0; c < 2; ++c) tld32(lane_base + st * 128 + 64 * hf + 32 * c, sc[c]);
         tld_wait();
       }
       fence_before();
       bar_arrive(&sfree[st]);
-      uint32_t mw[4];
+      uint32_t mw[2];
       __all_sync(0xFFFFFFFFu, bar_wait(&mfull[st], (i >> 1) & 1));
 #pragma unroll
-      for (int c = 0; c < 4; ++c) mw[c] = maskrow[(st * kMaxG + g) * 4 + c];
+      for (int c = 0; c < 2; ++c) mw[c] = maskrow[(st * kMaxG + g) * 4 + 2 * hf + c];
       bar_arrive(&mempty[st]);
       // masked, scaled scores (base 2), kept in place, and their maximum
       // (four partial maxima keep the dependency chains short)
       float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+      for (int c = 0; c < 2; ++c)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float sv = (mw[c] & (1u << j)) ? __uint_as_float(sc[c][j]) * p.scale_log2 : -INFINITY;
           sc[c][j] = __float_as_uint(sv);
           tm[j & 3] = fmaxf(tm[j & 3], sv);
         }
-      const float m_new = fmaxf(m_used, fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3])));
+      // the row's maximum over both halves (both threads of the row then
+      // take identical decisions)
+      const float mine = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
+      xch[((i & 1) * 2 + hf) * 128 + r] = mine;
+      named_sync(pair_bar, 64);
+      const float other = xch[((i & 1) * 2 + (hf ^ 1)) * 128 + r];
+      const float m_new = fmaxf(m_used, fmaxf(mine, other));
       // the previous tile's P V is done: P may be rewritten, O rescaled
       if (i >= 1) {
         __all_sync(0xFFFFFFFFu, bar_wait(pvdone, (i - 1) & 1));
@@ -698,27 +706,28 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
         alpha = ex2(m_used - m_new);
       }
       if (__any_sync(0xFFFFFFFFu, alpha != 1.f) && i >= 1) {
-        // rescale this row of O (warp-wide TMEM access; rows without a change use 1)
+        // rescale this half of the row of O (warp-wide TMEM access; rows
+        // without a change use 1)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t ov[32];
-          tld32(lane_base + 256 + 32 * c, ov);
+          tld32(lane_base + 256 + 64 * hf + 32 * c, ov);
           tld_wait();
 #pragma unroll
           for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          tst32(lane_base + 256 + 32 * c, ov);
+          tst32(lane_base + 256 + 64 * hf + 32 * c, ov);
         }
         tst_wait();
       }
       l *= alpha;
       m_used = m_next;
-      // P row (bf16) into the swizzled A tile of the second MMA: 2^(s - m),
-      // zero for masked positions (2^-inf); a row with nothing selected yet
-      // writes zeros
+      // this half of the P row (bf16) into block hf of the swizzled A tile
+      // of the second MMA: 2^(s - m), zero for masked positions (2^-inf); a
+      // row with nothing selected yet writes zeros
       const bool any = m_used > -INFINITY;
       float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int q8 = 0; q8 < 4; ++q8) {
           uint32_t w[4];
@@ -730,7 +739,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
             ls[pr] += p0 + p1;
             w[pr] = pack_bf16x2(p0, p1);
           }
-          st16(sb + kOffP + sw_off(r, 4 * c + q8), make_uint4(w[0], w[1], w[2], w[3]));
+          st16(sb + kOffP + sw_off(r, 8 * hf + 4 * c + q8), make_uint4(w[0], w[1], w[2], w[3]));
         }
       }
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
@@ -738,20 +747,25 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       fence_before();
       bar_arrive(pfull);
     }
-    // the last P V, then this row's output
+    // the last P V, then this half of the row's output; the row's sum is the
+    // two halves' sums (added in the same order by both)
     bool done = true;
     if (ntiles > 0) {
       done = __all_sync(0xFFFFFFFFu, bar_wait(pvdone, (ntiles - 1) & 1));
       fence_after();
     }
+    xch[((ntiles & 1) * 2 + hf) * 128 + r] = l;
+    named_sync(pair_bar, 64);
+    const float l_other = xch[((ntiles & 1) * 2 + (hf ^ 1)) * 128 + r];
+    l = hf == 0 ? l + l_other : l_other + l;
     const bool real = t < p.T;
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    float* orow = p.o + ((int64_t)t * p.H + h) * kDim;
+    float* orow = p.o + ((int64_t)t * p.H + h) * kDim + 64 * hf;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 2; ++c) {
       uint32_t ov[32];
       if (ntiles > 0 && done) {
-        tld32(lane_base + 256 + 32 * c, ov);
+        tld32(lane_base + 256 + 64 * hf + 32 * c, ov);
         tld_wait();
       }
       if (real) {
@@ -766,7 +780,8 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
         }
       }
     }
-    if (real) p.lse[(int64_t)t * p.H + h] = l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
+    if (real && hf == 0)
+      p.lse[(int64_t)t * p.H + h] = l > 0.f ? (m_used + log2f(l)) * 0.6931471805599453f : -INFINITY;
   }
   fence_before();
   __syncthreads();
@@ -847,6 +862,13 @@ int dsa_sparse_attention(const dsa_attention_cfg* cfg, const uint16_t* q, const 
       cudaGetLastError();
       return DSA_ERR_CUDA;
     }
+    // the register split needs the whole launch allocation it was sized for
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, attention_kernel) != cudaSuccess) {
+      cudaGetLastError();
+      return DSA_ERR_CUDA;
+    }
+    if (fa.numRegs < kALaunchRegs) return DSA_ERR_UNSUPPORTED;
     configured = true;
   }
   AttnParams P;
