@@ -486,7 +486,13 @@ def measure_fused(dsa, torch, dev, T=608, S=131072, B=8, Kb=256, K=2048):
 
 def measure_attention(dsa, torch, dev, T=2048, H=8, S=1 << 20, Kc=2048, own=0.05):
     """Grouped masked sparse attention (dsa_sparse_attention): union build plus
-    attention, on T tokens whose neighbours share most of their selection."""
+    attention, on T tokens whose neighbours share most of their selection.
+
+    The path is bound by HBM: every union position's key and value rows
+    (2 x 256 bytes) are gathered once per group.  Algorithmic bytes: the
+    union reads the selections and writes each group's record (count, keys,
+    masks); the attention reads the records, Q and the gathered rows and
+    writes o and lse."""
     q, k, v, idx = wk.attention_inputs(T, H, S, Kc, seed=21, own=own, G=128 // H)
     qd, kd, vd = (torch.from_numpy(x.view(np.int16)).to(dev) for x in (q, k, v))
     idd = torch.from_numpy(idx).to(dev)
@@ -495,15 +501,20 @@ def measure_attention(dsa, torch, dev, T=2048, H=8, S=1 << 20, Kc=2048, own=0.05
     o = torch.empty((T, H, 128), dtype=torch.float32, device=dev)
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
     scale = 1.0 / math.sqrt(128)
-    for _ in range(3):
-        dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse)
-    e0, e1 = _events(torch, 2)
-    e0.record()
-    for _ in range(10):
-        dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse)
-    e1.record()
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / 10
+
+    def timed(f, reps=20):
+        for _ in range(3):
+            f()
+        e0, e1 = _events(torch, 2)
+        e0.record()
+        for _ in range(reps):
+            f()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    us_union = timed(lambda: dsa.dsa_group_union(cfg, idd, ws))
+    us = timed(lambda: dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse))
     G = 128 // H
     groups = -(-T // G)
     cap = G * Kc
@@ -513,16 +524,28 @@ def measure_attention(dsa, torch, dev, T=2048, H=8, S=1 << 20, Kc=2048, own=0.05
     sel = (idx >= 0).sum(axis=1)
     useful = 2.0 * H * float(sel.sum()) * (128 + 128)
     tiles = np.ceil(union / 128.0)
-    executed = 2.0 * groups * 128 * float((tiles * 128).sum() / groups) * (128 + 128)
+    executed = 2.0 * 128 * float((tiles * 128).sum()) * (128 + 128)
+    u_tot = float(union.sum())
+    union_bytes = 4.0 * T * Kc + groups * 16 + 8.0 * u_tot
+    attn_bytes = 4.0 + 8.0 * u_tot + T * H * 128 * 2 + 2 * 256 * u_tot + T * H * (128 * 4 + 4)
+    hbm, hbm_src = hbm_peak()
     peak = None
     try:
         with open(PEAKS) as f:
             peak = float(json.load(f)["bf16_tflops"])
     except Exception:
         peak = 1900.0
+    us_attn = us - us_union
     return {"tokens": T, "heads": H, "group": G, "keys": S, "select": Kc, "neighbour_own_fraction": own,
-            "us_per_call": us, "tokens_per_s": T / (us * 1e-6),
+            "us_per_call": us, "us_union": us_union, "us_attention": us_attn,
+            "tokens_per_s": T / (us * 1e-6),
             "union_over_selection": float(union.mean() / sel.mean()),
+            "roofline": {"bound": "hbm", "unit": "GB/s", "peak": hbm, "peak_source": hbm_src,
+                         "bytes_per_call": union_bytes + attn_bytes,
+                         "achieved": (union_bytes + attn_bytes) / (us * 1e-6) / 1e9,
+                         "frac": (union_bytes + attn_bytes) / (us * 1e-6) / 1e9 / hbm,
+                         "attention_kernel_frac": attn_bytes / (us_attn * 1e-6) / 1e9 / hbm,
+                         "union_kernel_frac": union_bytes / (us_union * 1e-6) / 1e9 / hbm},
             "useful_tflops": useful / (us * 1e-6) / 1e12, "executed_tflops": executed / (us * 1e-6) / 1e12,
             "bf16_peak_tflops": peak, "status": dsa.dsa_sparse_attention_status()}
 
