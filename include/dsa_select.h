@@ -238,7 +238,7 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
                        struct CUstream_st* stream);
 
 /*
- * Grouped masked sparse attention over the selection (SURVEY NEXT-4).
+ * Grouped masked sparse attention over the selection.
  *
  * vLLM PR #48726 ("LiteDSA: grouped masked sparse attention"): with H query
  * heads per token, G = 128 / H adjacent tokens form a group whose G x H

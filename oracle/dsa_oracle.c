@@ -364,7 +364,7 @@ int oracle_indexer_logits(const uint8_t* q, const uint8_t* k, const float* k_sca
 }
 
 /* ---------------------------------------------------------------------------
- * NEXT-4: grouped masked sparse attention over the union of neighbouring
+ * Grouped masked sparse attention over the union of neighbouring
  * queries' selections.
  *
  * [P2] vLLM PR #48726, "LiteDSA: grouped masked sparse attention": with H

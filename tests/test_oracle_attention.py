@@ -1,4 +1,4 @@
-"""Pins of the grouped sparse attention oracle (NEXT-4) against what the
+"""Pins of the grouped sparse attention oracle against what the
 mathematics fixes: softmax over one position, softmax of equal scores,
 an independent numpy formulation on small inputs, order independence,
 empty selections, and the union against Python sets."""

@@ -297,7 +297,7 @@ def indexer_inputs(T: int, S: int, seed: int = 7, heads: int = 64, dim: int = 12
 
 
 # ---------------------------------------------------------------------------
-# grouped sparse attention (NEXT-4) inputs
+# grouped sparse attention inputs
 
 _S_AQ = 121
 _S_AK = 122
