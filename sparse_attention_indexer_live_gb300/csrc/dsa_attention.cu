@@ -282,16 +282,18 @@ constexpr int kDim = 128;              // head_dim = value_dim
 constexpr int kBlk = 128 * 128;        // one 128-row x 128-byte swizzled block
 constexpr int kOffQ = 0;               // Q: 2 blocks (dims 0-63, 64-127)
 constexpr int kOffK = kOffQ + 2 * kBlk;            // K: 2 stages x 2 blocks
-constexpr int kOffV = kOffK + 4 * kBlk;            // V: 2 stages x 2 blocks (dims 0-63, 64-127), like K
-constexpr int kOffP = kOffV + 4 * kBlk;            // P: 2 blocks (keys 0-63, 64-127)
-constexpr int kOffMask = kOffP + 2 * kBlk;         // per stage, per token: 4 words (128 positions)
+constexpr int kVStages = 3;
+constexpr int kOffV = kOffK + 4 * kBlk;            // V: 3 stages x 2 blocks (dims 0-63, 64-127), like K
+constexpr int kOffMask = kOffV + 2 * kVStages * kBlk;  // per stage, per token: 4 words (128 positions)
 constexpr int kMaxG = 16;
 constexpr int kOffXch = kOffMask + 2 * kMaxG * 4 * 4;  // [tile parity][half][row] partial row maxima
 constexpr int kOffBarA = kOffXch + 2 * 2 * 128 * 4;
-constexpr int kNumBarsA = 19;
+constexpr int kNumBarsA = 23;
 constexpr int kOffTmemA = kOffBarA + kNumBarsA * 8;
 constexpr int kSmemA = kOffTmemA + 16 + 1024;       // + slack for the 1024-byte alignment
-constexpr uint32_t kTmemColsA = 512;               // S buffers at 0 and 128, O at 256
+constexpr uint32_t kTmemColsA = 512;               // S buffers at 0 and 128, O at 256, P at 384 and 448
+constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;                   // bf16 pairs: 64 columns = 128 positions per row
 // f32 accumulator, A = B = bf16, both K-major, N = 128, M = 128.
 constexpr uint32_t kIdescA = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
                              ((uint32_t)(128 >> 4) << 24);
@@ -411,20 +413,20 @@ __device__ __forceinline__ uint64_t sdesc_nmajor(uint32_t a) {
 }
 constexpr uint32_t kIdescPV = kIdescA | (1u << 16);  // B N-major
 
-// O (+)= P V over K = 128 positions (eight K = 16 steps of 16 rows of V).
-__device__ __forceinline__ void mma_pv(uint32_t d, uint32_t a, uint32_t b, bool acc) {
+// O (+)= P V over K = 128 positions (eight K = 16 steps of 16 rows of V),
+// with P in tensor memory: row m in lane m, positions 2c and 2c + 1 as the
+// bf16 pair of column c, so each K step reads the next 8 columns.
+__device__ __forceinline__ void mma_pv(uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint64_t ad = sdesc(a + (uint32_t)((kk >> 2) * kBlk + (kk & 3) * 32));
     const uint64_t bd = sdesc_nmajor(b + (uint32_t)(kk * 16 * 128));
     const uint32_t en = (acc || kk > 0) ? 1u : 0u;
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-        "l"(ad), "l"(bd), "r"(kIdescPV), "r"(en));
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
+        "r"(a_tmem + 8 * kk), "l"(bd), "r"(kIdescPV), "r"(en));
   }
 }
-__device__ __forceinline__ void cp_wait_1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -456,6 +458,14 @@ __device__ __forceinline__ void tst32(uint32_t addr, const uint32_t (&r)[32]) {
       "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+__device__ __forceinline__ void tst16(uint32_t addr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          addr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+      "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
 __device__ __forceinline__ void tld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tst_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -484,14 +494,14 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   uint64_t* qfull = bars;
   uint64_t* kfull = bars + 1;    // [2] K tile loaded (K loaders)
   uint64_t* kempty = bars + 3;   // [2] S of that tile done (MMA commit)
-  uint64_t* vfull = bars + 5;    // [2] V tile loaded (V loaders)
-  uint64_t* vempty = bars + 7;   // [2] P V of that tile done (MMA commit)
-  uint64_t* mfull = bars + 9;    // [2] token masks written (mask warp)
-  uint64_t* mempty = bars + 11;  // [2] masks read (softmax)
-  uint64_t* sfull = bars + 13;   // [2] S in TMEM (MMA commit)
-  uint64_t* sfree = bars + 15;   // [2] S read (softmax)
-  uint64_t* pfull = bars + 17;   // P written (softmax)
-  uint64_t* pvdone = bars + 18;  // P V done (MMA commit)
+  uint64_t* vfull = bars + 5;    // [3] V tile loaded (V loaders)
+  uint64_t* vempty = bars + 8;   // [3] P V of that tile done (MMA commit)
+  uint64_t* mfull = bars + 11;   // [2] token masks written (mask warp)
+  uint64_t* mempty = bars + 13;  // [2] masks read (softmax)
+  uint64_t* sfull = bars + 15;   // [2] S in TMEM (MMA commit)
+  uint64_t* sfree = bars + 17;   // [2] S read (softmax)
+  uint64_t* pfull = bars + 19;   // [2] P of the tile written to its TMEM buffer (softmax)
+  uint64_t* pvdone = bars + 21;  // [2] P V of the tile done (MMA commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + kOffTmemA);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -507,18 +517,20 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   if (threadIdx.x == 0) {
     s_attn_abort = 0;
     bar_init(qfull, 64);
+    for (int i = 0; i < kVStages; ++i) {
+      bar_init(&vfull[i], 64);
+      bar_init(&vempty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
       bar_init(&kfull[i], 64);
       bar_init(&kempty[i], 1);
-      bar_init(&vfull[i], 64);
-      bar_init(&vempty[i], 1);
       bar_init(&mfull[i], 32);
       bar_init(&mempty[i], 256);
       bar_init(&sfull[i], 1);
       bar_init(&sfree[i], 256);
+      bar_init(&pfull[i], 256);
+      bar_init(&pvdone[i], 1);
     }
-    bar_init(pfull, 256);
-    bar_init(pvdone, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 4) {
@@ -534,13 +546,15 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   if (warp < 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLoadRegs));
     if (warp < 4) {
-      // ---- loaders: warps 0-1 Q and K, warps 2-3 V.  Warp w of a pair owns
-      // rows 64 w .. 64 w + 63 of each tile; one copy instruction moves two
-      // whole rows (a half-warp per 256-byte row, 16 bytes a lane), so every
-      // request is a full row.  Lane l holds the keys of rows 2 l and 2 l + 1
-      // of its warp's share and hands them round by shuffles.  Two tiles stay
-      // in flight: tile i is announced once tile i + 1 has been issued.
+      // ---- loaders: warps 0-1 Q and K (2 stages), warps 2-3 V (3 stages).
+      // Warp w of a pair owns rows 64 w .. 64 w + 63 of each tile; one copy
+      // instruction moves two whole rows (a half-warp per 256-byte row, 16
+      // bytes a lane), so every request is a full row.  Lane l holds the keys
+      // of rows 2 l and 2 l + 1 of its warp's share and hands them round by
+      // shuffles.  A tile is announced as soon as it has landed, so a stage's
+      // consumer never waits for the loader to get the next stage.
       const bool is_k = warp < 2;
+      const int nst = is_k ? 2 : kVStages;
       const int wrow = 64 * (warp & 1);       // first row of this warp's share
       const int half = lane >> 4, c = lane & 15;
       const uint16_t* rows_src = is_k ? p.k : p.v;
@@ -562,32 +576,31 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       }
       int32_t ck0 = wrow + 2 * lane < n ? ukeys[wrow + 2 * lane] : -1;
       int32_t ck1 = wrow + 2 * lane + 1 < n ? ukeys[wrow + 2 * lane + 1] : -1;
-      for (int i = 0; i <= ntiles; ++i) {
-        if (i < ntiles) {
-          const int st = i & 1;
-          if (i >= 2 && !bar_wait(&empty[st], ((i >> 1) & 1) ^ 1)) break;
-          const uint32_t dst = tile_base + st * 2 * kBlk;
+      int st = 0, use = 0;  // stage of tile i and how often it was used before
+      for (int i = 0; i < ntiles; ++i) {
+        if (i >= nst && !bar_wait(&empty[st], (use & 1) ^ 1)) break;
+        const uint32_t dst = tile_base + st * 2 * kBlk;
 #pragma unroll 8
-          for (int j = 0; j < 32; ++j) {
-            const int32_t k0 = __shfl_sync(0xFFFFFFFFu, ck0, j);
-            const int32_t k1 = __shfl_sync(0xFFFFFFFFu, ck1, j);
-            const int32_t key = half ? k1 : k0;
-            const int row = wrow + 2 * j + half;
-            if (key >= 0)
-              cp16(dst + sw_off(row, c), rows_src + (int64_t)key * kDim + 8 * c);
-            else
-              st16(dst + sw_off(row, c), make_uint4(0, 0, 0, 0));
-          }
-          cp_commit();
-          const int e = (i + 1) * kTileN + wrow + 2 * lane;
-          ck0 = e < n ? ukeys[e] : -1;
-          ck1 = e + 1 < n ? ukeys[e + 1] : -1;
+        for (int j = 0; j < 32; ++j) {
+          const int32_t k0 = __shfl_sync(0xFFFFFFFFu, ck0, j);
+          const int32_t k1 = __shfl_sync(0xFFFFFFFFu, ck1, j);
+          const int32_t key = half ? k1 : k0;
+          const int row = wrow + 2 * j + half;
+          if (key >= 0)
+            cp16(dst + sw_off(row, c), rows_src + (int64_t)key * kDim + 8 * c);
+          else
+            st16(dst + sw_off(row, c), make_uint4(0, 0, 0, 0));
         }
-        if (i >= 1) {
-          // tile i - 1 has landed (only tile i may still be in flight)
-          if (i < ntiles) cp_wait_1(); else cp_wait_all();
-          fence_async_smem();
-          bar_arrive(&full[(i - 1) & 1]);
+        cp_commit();
+        const int e = (i + 1) * kTileN + wrow + 2 * lane;
+        ck0 = e < n ? ukeys[e] : -1;
+        ck1 = e + 1 < n ? ukeys[e + 1] : -1;
+        cp_wait_all();
+        fence_async_smem();
+        bar_arrive(&full[st]);
+        if (++st == nst) {
+          st = 0;
+          ++use;
         }
       }
       cp_wait_all();  // nothing of this thread still in flight (also after an abort)
@@ -620,12 +633,13 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       if (lane == 0 && ntiles > 0 && bar_wait(qfull, 0)) {
         bool ok = true;
         auto pv = [&](int j) {
-          if (!bar_wait(&vfull[j & 1], (j >> 1) & 1)) return false;
-          if (!bar_wait(pfull, j & 1)) return false;
+          const int vs = j % kVStages, vu = j / kVStages;
+          if (!bar_wait(&vfull[vs], vu & 1)) return false;
+          if (!bar_wait(&pfull[j & 1], (j >> 1) & 1)) return false;
           fence_after();
-          mma_pv(tmem + 256, sb + kOffP, sb + kOffV + (j & 1) * 2 * kBlk, j > 0);
-          mma_commit(pvdone);
-          mma_commit(&vempty[j & 1]);
+          mma_pv(tmem + kTmemO, tmem + kTmemP + 64 * (j & 1), sb + kOffV + vs * 2 * kBlk, j > 0);
+          mma_commit(&pvdone[j & 1]);
+          mma_commit(&vempty[vs]);
           return true;
         };
         for (int i = 0; i < ntiles && ok; ++i) {
@@ -670,88 +684,94 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
 #pragma unroll
       for (int c = 0; c < 2; ++c) mw[c] = maskrow[(st * kMaxG + g) * 4 + 2 * hf + c];
       bar_arrive(&mempty[st]);
-      // masked, scaled scores (base 2), kept in place, and their maximum
-      // (four partial maxima keep the dependency chains short)
-      float tm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      // masked scores: -inf where the token did not select the position
 #pragma unroll
       for (int c = 0; c < 2; ++c)
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float sv = (mw[c] & (1u << j)) ? __uint_as_float(sc[c][j]) * p.scale_log2 : -INFINITY;
-          sc[c][j] = __float_as_uint(sv);
-          tm[j & 3] = fmaxf(tm[j & 3], sv);
+        for (int j = 0; j < 32; ++j)
+          if (!(mw[c] & (1u << j))) sc[c][j] = __float_as_uint(-INFINITY);
+      // this tile's P buffer is free once the P V of two tiles back is done
+      if (i >= 2) {
+        __all_sync(0xFFFFFFFFu, bar_wait(&pvdone[st], ((i >> 1) & 1) ^ 1));
+        fence_after();
+      }
+      // One pass: weights 2^(s c - m) against the running maximum m, and the
+      // tile's maximum.  The maximum used for the weights moves only when the
+      // row's maximum rises by more than 8 (a factor 256): until then the
+      // weights stay below 256, and the final normalisation by the same m
+      // makes the result exact, so the pass is redone (and O rescaled) rarely
+      // -- always on a row's first tile with a selected position.
+      const float c2 = p.scale_log2;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float lsum;
+      // this half of the P row goes to 32 TMEM columns of bf16 pairs, 16 at a time
+      const uint32_t p_addr = lane_base + kTmemP + 64 * st + 32 * hf;
+      auto weights = [&](float m_eff, bool track) {
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float s0 = __uint_as_float(sc[c][j]), s1 = __uint_as_float(sc[c][j + 1]);
+            if (track) {
+              mx[j & 3] = fmaxf(mx[j & 3], s0);
+              mx[(j + 1) & 3] = fmaxf(mx[(j + 1) & 3], s1);
+            }
+            const float p0 = ex2(fmaf(s0, c2, -m_eff));
+            const float p1 = ex2(fmaf(s1, c2, -m_eff));
+            ls[j & 3] += p0;
+            ls[(j + 1) & 3] += p1;
+            pk[j / 2] = pack_bf16x2(p0, p1);
+          }
+          tst16(p_addr + 16 * c, pk);
         }
+        lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+      };
+      // before any selected position the weights are taken against 0 (all
+      // masked: zeros; otherwise the pass is redone below)
+      weights(m_used == -INFINITY ? 0.f : m_used, true);
       // the row's maximum over both halves (both threads of the row then
       // take identical decisions)
-      const float mine = fmaxf(fmaxf(tm[0], tm[1]), fmaxf(tm[2], tm[3]));
+      const float mine = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2;
       xch[((i & 1) * 2 + hf) * 128 + r] = mine;
       named_sync(pair_bar, 64);
       const float other = xch[((i & 1) * 2 + (hf ^ 1)) * 128 + r];
       const float m_new = fmaxf(m_used, fmaxf(mine, other));
-      // the previous tile's P V is done: P may be rewritten, O rescaled
-      if (i >= 1) {
-        __all_sync(0xFFFFFFFFu, bar_wait(pvdone, (i - 1) & 1));
-        fence_after();
-      }
-      // The running maximum used for the weights moves only when the row's
-      // maximum rises by more than 8 (a factor 256): until then the weights
-      // exp2(s - m_used) stay below 256, and the final normalisation by the
-      // same m_used makes the result exact, so O is rescaled rarely.
+      const bool redo = m_used == -INFINITY ? m_new > -INFINITY : m_new > m_used + 8.f;
       float alpha = 1.f;
-      float m_next = m_used;
-      if (m_used == -INFINITY) {
-        m_next = m_new;  // nothing accumulated yet: O and l are zero
-      } else if (m_new > m_used + 8.f) {
-        m_next = m_new;
-        alpha = ex2(m_used - m_new);
-      }
-      if (__any_sync(0xFFFFFFFFu, alpha != 1.f) && i >= 1) {
-        // rescale this half of the row of O (warp-wide TMEM access; rows
-        // without a change use 1)
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          uint32_t ov[32];
-          tld32(lane_base + 256 + 64 * hf + 32 * c, ov);
-          tld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-          tst32(lane_base + 256 + 64 * hf + 32 * c, ov);
+      if (__any_sync(0xFFFFFFFFu, redo)) {
+        if (redo) {
+          if (m_used > -INFINITY) alpha = ex2(m_used - m_new);
+          m_used = m_new;
         }
-        tst_wait();
-      }
-      l *= alpha;
-      m_used = m_next;
-      // this half of the P row (bf16) into block hf of the swizzled A tile
-      // of the second MMA: 2^(s - m), zero for masked positions (2^-inf); a
-      // row with nothing selected yet writes zeros
-      const bool any = m_used > -INFINITY;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // rows without a change recompute the same weights
+        weights(m_used == -INFINITY ? 0.f : m_used, false);
+        if (__any_sync(0xFFFFFFFFu, alpha != 1.f) && i >= 1) {
+          // rescale this half of the row of O once the previous P V is done
+          __all_sync(0xFFFFFFFFu, bar_wait(&pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1));
+          fence_after();
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 2; ++c) {
+            uint32_t ov[32];
+            tld32(lane_base + kTmemO + 64 * hf + 32 * c, ov);
+            tld_wait();
 #pragma unroll
-        for (int q8 = 0; q8 < 4; ++q8) {
-          uint32_t w[4];
-#pragma unroll
-          for (int pr = 0; pr < 4; ++pr) {
-            const int j = 8 * q8 + 2 * pr;
-            const float p0 = any ? ex2(__uint_as_float(sc[c][j]) - m_used) : 0.f;
-            const float p1 = any ? ex2(__uint_as_float(sc[c][j + 1]) - m_used) : 0.f;
-            ls[pr] += p0 + p1;
-            w[pr] = pack_bf16x2(p0, p1);
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+            tst32(lane_base + kTmemO + 64 * hf + 32 * c, ov);
           }
-          st16(sb + kOffP + sw_off(r, 8 * hf + 4 * c + q8), make_uint4(w[0], w[1], w[2], w[3]));
         }
       }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      fence_async_smem();
+      l = l * alpha + lsum;
+      tst_wait();
       fence_before();
-      bar_arrive(pfull);
+      bar_arrive(&pfull[st]);
     }
     // the last P V, then this half of the row's output; the row's sum is the
     // two halves' sums (added in the same order by both)
     bool done = true;
     if (ntiles > 0) {
-      done = __all_sync(0xFFFFFFFFu, bar_wait(pvdone, (ntiles - 1) & 1));
+      done = __all_sync(0xFFFFFFFFu, bar_wait(&pvdone[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1));
       fence_after();
     }
     xch[((ntiles & 1) * 2 + hf) * 128 + r] = l;
@@ -765,7 +785,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
     for (int c = 0; c < 2; ++c) {
       uint32_t ov[32];
       if (ntiles > 0 && done) {
-        tld32(lane_base + 256 + 64 * hf + 32 * c, ov);
+        tld32(lane_base + kTmemO + 64 * hf + 32 * c, ov);
         tld_wait();
       }
       if (real) {
