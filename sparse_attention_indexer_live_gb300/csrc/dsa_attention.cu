@@ -427,6 +427,11 @@ __device__ __forceinline__ void mma_pv(uint32_t d, uint32_t a_tmem, uint32_t b, 
         "r"(a_tmem + 8 * kk), "l"(bd), "r"(kIdescPV), "r"(en));
   }
 }
+// 16 bytes from src, or 16 zero bytes (src not read) when !valid
+__device__ __forceinline__ void cp16_zfill(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+               : "memory");
+}
 __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void named_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -518,11 +523,11 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
     s_attn_abort = 0;
     bar_init(qfull, 64);
     for (int i = 0; i < kVStages; ++i) {
-      bar_init(&vfull[i], 64);
+      bar_init(&vfull[i], 32);
       bar_init(&vempty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      bar_init(&kfull[i], 64);
+      bar_init(&kfull[i], 32);
       bar_init(&kempty[i], 1);
       bar_init(&mfull[i], 32);
       bar_init(&mempty[i], 256);
@@ -547,21 +552,21 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLoadRegs));
     if (warp < 4) {
       // ---- loaders: warps 0-1 Q and K (2 stages), warps 2-3 V (3 stages).
-      // Warp w of a pair owns rows 64 w .. 64 w + 63 of each tile; one copy
+      // Warps 0-1 first copy the Q tile.  Then each warp of a pair loads
+      // every other tile whole, so two tiles are in flight.  One copy
       // instruction moves two whole rows (a half-warp per 256-byte row, 16
-      // bytes a lane), so every request is a full row.  Lane l holds the keys
-      // of rows 2 l and 2 l + 1 of its warp's share and hands them round by
-      // shuffles.  A tile is announced as soon as it has landed, so a stage's
-      // consumer never waits for the loader to get the next stage.
+      // bytes a lane), so every request is a full row; positions past the
+      // union are zero-filled by the same copy (source size 0).  A tile is
+      // announced (32 arrivals) as soon as it has landed.
       const bool is_k = warp < 2;
       const int nst = is_k ? 2 : kVStages;
-      const int wrow = 64 * (warp & 1);       // first row of this warp's share
       const int half = lane >> 4, c = lane & 15;
       const uint16_t* rows_src = is_k ? p.k : p.v;
       uint64_t* full = is_k ? kfull : vfull;
       uint64_t* empty = is_k ? kempty : vempty;
       const uint32_t tile_base = sb + (is_k ? kOffK : kOffV);
       if (is_k) {
+        const int wrow = 64 * warp;
         for (int j = 0; j < 32; ++j) {
           const int row = wrow + 2 * j + half;
           const int64_t qr = (int64_t)t0 * p.H + row;  // query/head row
@@ -574,59 +579,76 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
         fence_async_smem();
         bar_arrive(qfull);
       }
-      int32_t ck0 = wrow + 2 * lane < n ? ukeys[wrow + 2 * lane] : -1;
-      int32_t ck1 = wrow + 2 * lane + 1 < n ? ukeys[wrow + 2 * lane + 1] : -1;
-      int st = 0, use = 0;  // stage of tile i and how often it was used before
-      for (int i = 0; i < ntiles; ++i) {
-        if (i >= nst && !bar_wait(&empty[st], (use & 1) ^ 1)) break;
+      // lane l holds the keys of rows l, 32 + l, 64 + l and 96 + l of its
+      // tile; copy j moves rows 2 j and 2 j + 1 (one shuffle: row 2 j + half)
+      const int first = warp & 1;  // this warp's tiles: first, first + 2, ...
+      int32_t ck[4];
+      auto keys = [&](int i) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int e = i * kTileN + 32 * u + lane;
+          ck[u] = e < n ? ukeys[e] : -1;
+        }
+      };
+      keys(first);
+      const uint16_t* src_c = rows_src + 8 * c;  // this lane's 16 bytes of a row
+      // swizzled offset of this lane's chunk in row 2 j + half: the pattern
+      // repeats every 4 copies (8 rows)
+      uint32_t soff[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) soff[j] = sw_off(2 * j + half, c);
+      for (int i = first; i < ntiles; i += 2) {
+        const int st = i % nst;
+        if (i >= nst && !bar_wait(&empty[st], ((i / nst) & 1) ^ 1)) break;
         const uint32_t dst = tile_base + st * 2 * kBlk;
-#pragma unroll 8
-        for (int j = 0; j < 32; ++j) {
-          const int32_t k0 = __shfl_sync(0xFFFFFFFFu, ck0, j);
-          const int32_t k1 = __shfl_sync(0xFFFFFFFFu, ck1, j);
-          const int32_t key = half ? k1 : k0;
-          const int row = wrow + 2 * j + half;
-          if (key >= 0)
-            cp16(dst + sw_off(row, c), rows_src + (int64_t)key * kDim + 8 * c);
-          else
-            st16(dst + sw_off(row, c), make_uint4(0, 0, 0, 0));
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int32_t key = __shfl_sync(0xFFFFFFFFu, ck[j >> 4], (2 * j + half) & 31);
+          cp16_zfill(dst + soff[j & 3] + (j >> 2) * 1024, src_c + (int64_t)max(key, 0) * kDim, key >= 0);
         }
         cp_commit();
-        const int e = (i + 1) * kTileN + wrow + 2 * lane;
-        ck0 = e < n ? ukeys[e] : -1;
-        ck1 = e + 1 < n ? ukeys[e + 1] : -1;
+        keys(i + 2);
         cp_wait_all();
         fence_async_smem();
         bar_arrive(&full[st]);
-        if (++st == nst) {
-          st = 0;
-          ++use;
-        }
       }
       cp_wait_all();  // nothing of this thread still in flight (also after an abort)
     } else if (warp == 5) {
       // ---- mask warp: the tile's token masks, one 128-bit row per token;
-      // the next tile's masks are read while this one's are written
-      uint32_t cm[4], nm[4];
-#pragma unroll
-      for (int w = 0; w < 4; ++w) cm[w] = 32 * w + lane < n ? umasks[32 * w + lane] : 0u;
-      for (int i = 0; i < ntiles; ++i) {
-        const int st = i & 1;
+      // the masks of the tile two ahead are read while this one's are written
+      uint32_t cm[4], nm[4], fm[4];
+      auto masks = [&](int i, uint32_t (&m)[4]) {
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-          const int e = (i + 1) * kTileN + 32 * w + lane;
-          nm[w] = e < n ? umasks[e] : 0u;
+          const int e = i * kTileN + 32 * w + lane;
+          m[w] = e < n ? umasks[e] : 0u;
         }
+      };
+      masks(0, cm);
+      masks(1, nm);
+      for (int i = 0; i < ntiles; ++i) {
+        const int st = i & 1;
+        masks(i + 2, fm);
         if (i >= 2 && !bar_wait(&mempty[st], ((i >> 1) & 1) ^ 1)) break;
+        // word w of token g: bit l = token g selected position 32 w + l;
+        // lane g keeps token g's word (16 ballots, unrolled; tokens past G
+        // have no bits)
 #pragma unroll
-        for (int w = 0; w < 4; ++w)
-          for (int g = 0; g < G; ++g) {
-            const uint32_t bit = __ballot_sync(0xFFFFFFFFu, (cm[w] >> g) & 1u);
-            if (lane == 0) maskrow[(st * kMaxG + g) * 4 + w] = bit;
+        for (int w = 0; w < 4; ++w) {
+          uint32_t mine = 0;
+#pragma unroll
+          for (int g = 0; g < kMaxG; ++g) {
+            const uint32_t bits = __ballot_sync(0xFFFFFFFFu, (cm[w] >> g) & 1u);
+            if (lane == g) mine = bits;
           }
+          if (lane < G) maskrow[(st * kMaxG + lane) * 4 + w] = mine;
+        }
         bar_arrive(&mfull[st]);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) cm[w] = nm[w];
+        for (int w = 0; w < 4; ++w) {
+          cm[w] = nm[w];
+          nm[w] = fm[w];
+        }
       }
     } else if (warp == 4) {
       // ---- MMA issuer
