@@ -288,12 +288,12 @@ constexpr int kOffMask = kOffV + 2 * kVStages * kBlk;  // per stage, per token: 
 constexpr int kMaxG = 16;
 constexpr int kOffXch = kOffMask + 2 * kMaxG * 4 * 4;  // [tile parity][half][row] partial row maxima
 constexpr int kOffBarA = kOffXch + 2 * 2 * 128 * 4;
-constexpr int kNumBarsA = 23;
+constexpr int kNumBarsA = 24;
 constexpr int kOffTmemA = kOffBarA + kNumBarsA * 8;
 constexpr int kSmemA = kOffTmemA + 16 + 1024;       // + slack for the 1024-byte alignment
-constexpr uint32_t kTmemColsA = 512;               // S buffers at 0 and 128, O at 256, P at 384 and 448
-constexpr uint32_t kTmemO = 256;
-constexpr uint32_t kTmemP = 384;                   // bf16 pairs: 64 columns = 128 positions per row
+constexpr uint32_t kTmemColsA = 512;               // S buffers at 0, 128 and 256, O at 384
+constexpr int kSStages = 3;
+constexpr uint32_t kTmemO = 384;
 // f32 accumulator, A = B = bf16, both K-major, N = 128, M = 128.
 constexpr uint32_t kIdescA = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(128 >> 3) << 17) |
                              ((uint32_t)(128 >> 4) << 24);
@@ -414,17 +414,20 @@ __device__ __forceinline__ uint64_t sdesc_nmajor(uint32_t a) {
 constexpr uint32_t kIdescPV = kIdescA | (1u << 16);  // B N-major
 
 // O (+)= P V over K = 128 positions (eight K = 16 steps of 16 rows of V),
-// with P in tensor memory: row m in lane m, positions 2c and 2c + 1 as the
-// bf16 pair of column c, so each K step reads the next 8 columns.
+// with P in tensor memory, in the columns of the S buffer it was computed
+// from: row m in lane m, positions 2c and 2c + 1 of the first half as the
+// bf16 pair of column c (columns 0-31), the second half's in columns 64-95
+// (each softmax half writes over scores only it has read).
 __device__ __forceinline__ void mma_pv(uint32_t d, uint32_t a_tmem, uint32_t b, bool acc) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
     const uint64_t bd = sdesc_nmajor(b + (uint32_t)(kk * 16 * 128));
     const uint32_t en = (acc || kk > 0) ? 1u : 0u;
+    const uint32_t a = a_tmem + (kk < 4 ? 8 * kk : 64 + 8 * (kk - 4));
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d),
-        "r"(a_tmem + 8 * kk), "l"(bd), "r"(kIdescPV), "r"(en));
+        "r"(a), "l"(bd), "r"(kIdescPV), "r"(en));
   }
 }
 // 16 bytes from src, or 16 zero bytes (src not read) when !valid
@@ -503,10 +506,9 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   uint64_t* vempty = bars + 8;   // [3] P V of that tile done (MMA commit)
   uint64_t* mfull = bars + 11;   // [2] token masks written (mask warp)
   uint64_t* mempty = bars + 13;  // [2] masks read (softmax)
-  uint64_t* sfull = bars + 15;   // [2] S in TMEM (MMA commit)
-  uint64_t* sfree = bars + 17;   // [2] S read (softmax)
-  uint64_t* pfull = bars + 19;   // [2] P of the tile written to its TMEM buffer (softmax)
-  uint64_t* pvdone = bars + 21;  // [2] P V of the tile done (MMA commit)
+  uint64_t* sfull = bars + 15;   // [3] S in TMEM buffer (MMA commit)
+  uint64_t* pfull = bars + 18;   // [3] P written over that buffer (softmax)
+  uint64_t* pvdone = bars + 21;  // [3] P V of that buffer done: buffer free (MMA commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + kOffTmemA);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -531,8 +533,9 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       bar_init(&kempty[i], 1);
       bar_init(&mfull[i], 32);
       bar_init(&mempty[i], 256);
+    }
+    for (int i = 0; i < kSStages; ++i) {
       bar_init(&sfull[i], 1);
-      bar_init(&sfree[i], 256);
       bar_init(&pfull[i], 256);
       bar_init(&pvdone[i], 1);
     }
@@ -654,27 +657,32 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       // ---- MMA issuer
       if (lane == 0 && ntiles > 0 && bar_wait(qfull, 0)) {
         bool ok = true;
+        // S runs two tiles ahead of P V: S(i) is issued before P V(i - 2).
+        // S(i) reuses the buffer of tile i - 3, whose P the P V of tile
+        // i - 3 read: it waits for that product.
         auto pv = [&](int j) {
           const int vs = j % kVStages, vu = j / kVStages;
+          const int ss = j % kSStages, su = j / kSStages;
           if (!bar_wait(&vfull[vs], vu & 1)) return false;
-          if (!bar_wait(&pfull[j & 1], (j >> 1) & 1)) return false;
+          if (!bar_wait(&pfull[ss], su & 1)) return false;
           fence_after();
-          mma_pv(tmem + kTmemO, tmem + kTmemP + 64 * (j & 1), sb + kOffV + vs * 2 * kBlk, j > 0);
-          mma_commit(&pvdone[j & 1]);
+          mma_pv(tmem + kTmemO, tmem + ss * 128, sb + kOffV + vs * 2 * kBlk, j > 0);
+          mma_commit(&pvdone[ss]);
           mma_commit(&vempty[vs]);
           return true;
         };
         for (int i = 0; i < ntiles && ok; ++i) {
-          const int st = i & 1;
-          if (!bar_wait(&kfull[st], (i >> 1) & 1)) break;
-          if (i >= 2 && !bar_wait(&sfree[st], ((i >> 1) & 1) ^ 1)) break;
+          const int kst = i & 1;
+          const int ss = i % kSStages, su = i / kSStages;
+          if (!bar_wait(&kfull[kst], (i >> 1) & 1)) break;
+          if (i >= kSStages && !bar_wait(&pvdone[ss], (su & 1) ^ 1)) break;
           fence_after();
-          mma_128(tmem + st * 128, sb + kOffQ, sb + kOffK + st * 2 * kBlk, false);
-          mma_commit(&sfull[st]);
-          mma_commit(&kempty[st]);
-          if (i >= 1) ok = pv(i - 1);
+          mma_128(tmem + ss * 128, sb + kOffQ, sb + kOffK + kst * 2 * kBlk, false);
+          mma_commit(&sfull[ss]);
+          mma_commit(&kempty[kst]);
+          if (i >= 2) ok = pv(i - 2);
         }
-        if (ok) pv(ntiles - 1);
+        for (int j = ntiles >= 2 ? ntiles - 2 : 0; j < ntiles && ok; ++j) ok = pv(j);
       }
     }
   } else {
@@ -690,17 +698,16 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
     const uint32_t lane_base = tmem + ((uint32_t)((sw & 3) * 32) << 16);
     float m_used = -INFINITY, l = 0.f;
     for (int i = 0; i < ntiles; ++i) {
-      const int st = i & 1;
-      const bool okw = __all_sync(0xFFFFFFFFu, bar_wait(&sfull[st], (i >> 1) & 1));
+      const int st = i & 1;                       // mask stage
+      const int ss = i % kSStages, su = i / kSStages;  // S / P buffer
+      const bool okw = __all_sync(0xFFFFFFFFu, bar_wait(&sfull[ss], su & 1));
       fence_after();
       uint32_t sc[2][32];
       if (okw) {
 #pragma unroll
-        for (int c = 0; c < 2; ++c) tld32(lane_base + st * 128 + 64 * hf + 32 * c, sc[c]);
+        for (int c = 0; c < 2; ++c) tld32(lane_base + ss * 128 + 64 * hf + 32 * c, sc[c]);
         tld_wait();
       }
-      fence_before();
-      bar_arrive(&sfree[st]);
       uint32_t mw[2];
       __all_sync(0xFFFFFFFFu, bar_wait(&mfull[st], (i >> 1) & 1));
 #pragma unroll
@@ -712,11 +719,6 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if (!(mw[c] & (1u << j))) sc[c][j] = __float_as_uint(-INFINITY);
-      // this tile's P buffer is free once the P V of two tiles back is done
-      if (i >= 2) {
-        __all_sync(0xFFFFFFFFu, bar_wait(&pvdone[st], ((i >> 1) & 1) ^ 1));
-        fence_after();
-      }
       // One pass: weights 2^(s c - m) against the running maximum m, and the
       // tile's maximum.  The maximum used for the weights moves only when the
       // row's maximum rises by more than 8 (a factor 256): until then the
@@ -726,8 +728,9 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       const float c2 = p.scale_log2;
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       float lsum;
-      // this half of the P row goes to 32 TMEM columns of bf16 pairs, 16 at a time
-      const uint32_t p_addr = lane_base + kTmemP + 64 * st + 32 * hf;
+      // this half of the P row goes over this half's scores in the S
+      // buffer: 32 TMEM columns of bf16 pairs, 16 at a time
+      const uint32_t p_addr = lane_base + ss * 128 + 64 * hf;
       auto weights = [&](float m_eff, bool track) {
         float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -771,7 +774,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
         weights(m_used == -INFINITY ? 0.f : m_used, false);
         if (__any_sync(0xFFFFFFFFu, alpha != 1.f) && i >= 1) {
           // rescale this half of the row of O once the previous P V is done
-          __all_sync(0xFFFFFFFFu, bar_wait(&pvdone[(i - 1) & 1], ((i - 1) >> 1) & 1));
+          __all_sync(0xFFFFFFFFu, bar_wait(&pvdone[(i - 1) % kSStages], ((i - 1) / kSStages) & 1));
           fence_after();
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
@@ -787,13 +790,13 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       l = l * alpha + lsum;
       tst_wait();
       fence_before();
-      bar_arrive(&pfull[st]);
+      bar_arrive(&pfull[ss]);
     }
     // the last P V, then this half of the row's output; the row's sum is the
     // two halves' sums (added in the same order by both)
     bool done = true;
     if (ntiles > 0) {
-      done = __all_sync(0xFFFFFFFFu, bar_wait(&pvdone[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1));
+      done = __all_sync(0xFFFFFFFFu, bar_wait(&pvdone[(ntiles - 1) % kSStages], ((ntiles - 1) / kSStages) & 1));
       fence_after();
     }
     xch[((ntiles & 1) * 2 + hf) * 128 + r] = l;
