@@ -133,6 +133,45 @@ def test_widest_group_rows():
     _run(16, 16, 1 << 18, 6144, seed=6, own=0.3)
 
 
+def test_graph_replay_follows_new_selections():
+    # both launches take their grids from the shapes only: a captured call
+    # replays on new selections (written into the captured buffers) and gives
+    # what a direct call gives
+    torch = _torch()
+    import sparse_attention_indexer_live_gb300 as dsa
+    T, H, S, Kc = 40, 8, 20000, 256
+    q, k, v, idx0 = wk.attention_inputs(T, H, S, Kc, seed=10, own=0.2)
+    _, _, _, idx1 = wk.attention_inputs(T, H, S, Kc, seed=11, own=0.6, fill=0.7)
+    dev = "cuda:0"
+    qd, kd, vd = (torch.from_numpy(x.view(np.int16)).to(dev) for x in (q, k, v))
+    idd = torch.from_numpy(idx0).to(dev)
+    cfg = dsa.attention_cfg(qd, kd, idd)
+    ws = torch.zeros(dsa.dsa_sparse_attention_workspace(cfg), dtype=torch.uint8, device=dev)
+    o = torch.empty((T, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(128)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse, stream=stream)  # warm-up
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse, stream=stream)
+    for sel in (idx1, idx0):
+        idd.copy_(torch.from_numpy(sel))
+        graph.replay()
+        torch.cuda.synchronize()
+        og, lg = o.clone(), lse.clone()
+        dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse)
+        torch.cuda.synchronize()
+        assert torch.equal(og, o) and torch.equal(lg, lse)
+    assert dsa.dsa_sparse_attention_status() == dsa.DSA_OK
+    # and the replayed result is the oracle's (selection idx0)
+    o_ref, lse_ref = oracle_default().sparse_attention(q, k, v, idx0, scale)
+    assert np.abs(og.cpu().numpy() - o_ref).max() <= 2.0 ** -8 * np.abs(_f(v)).max() + 1e-5
+    assert np.abs(lg.cpu().numpy() - lse_ref).max() <= 1e-4 + 1e-5 * np.abs(lse_ref).max()
+
+
 def test_unsupported_shapes():
     torch = _torch()
     import sparse_attention_indexer_live_gb300 as dsa
