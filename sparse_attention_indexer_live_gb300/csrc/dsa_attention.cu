@@ -9,20 +9,23 @@
 // tokens that selected each) and the attention over it.
 //
 // Design (this file's own):
-//   * union: one CTA per group stages the group's rows in shared memory and
-//     merges them, each thread a slice of the key range (no atomics);
+//   * union: one CTA per group stages the group's rows in shared memory, cuts
+//     key space into 512 ranges (one per thread) and merges each range's
+//     pieces of the rows once, with the rows' heads in registers; output goes
+//     to provisional slots and is compacted after a block-wide prefix (no
+//     atomics);
 //   * attention: one CTA per group of 128 query/head rows, walking the union
-//     in tiles of 128 positions: two warps gather the tile's key rows into the
-//     128B-swizzled K-major layout the tensor cores read (cp.async), four write
-//     the value rows transposed (8 x 8 transposes in registers) and one the
-//     tile's token masks, each with its own double-buffered barriers, so a
-//     score tile never waits for value loads;
-//     one thread issues tcgen05.mma (bf16, fp32 accumulators in TMEM) for
-//     S = Q K^T (two TMEM buffers, so the next tile's scores are computed
-//     while this one is normalised) and O += P V; four softmax warps, one
-//     row each, apply the token's selection mask, keep the running maximum
-//     and sum, rescale O in TMEM when the maximum rises, and write P as bf16
-//     for the second MMA.  Every mbarrier wait is bounded by a clock limit.
+//     in tiles of 128 positions.  Loader warps gather the tile's key and
+//     value rows (cp.async, whole 256-byte rows per half-warp, two tiles in
+//     flight) into the 128B-swizzled layout the tensor cores read; a mask
+//     warp expands the tile's token masks; one thread issues tcgen05.mma
+//     (bf16, fp32 accumulators in TMEM): S = Q K^T into one of three TMEM
+//     buffers, two tiles ahead, and O += P V with P read from tensor memory
+//     and V untransposed as an N-major operand; two softmax warpgroups, each
+//     half of the columns of every row, apply the masks, keep the running
+//     maximum and sum in one pass, rescale O rarely, and write P as bf16 over
+//     the scores it came from.  Every mbarrier wait is bounded by a clock
+//     limit.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
