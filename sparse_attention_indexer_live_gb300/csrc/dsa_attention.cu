@@ -488,6 +488,26 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Packed pairs of fp32 (one instruction for two lanes' worth of work).
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 // lo and hi rounded to bf16 (nearest even), lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -735,26 +755,37 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       // buffer: 32 TMEM columns of bf16 pairs, 16 at a time
       const uint32_t p_addr = lane_base + ss * 128 + 64 * hf;
       auto weights = [&](float m_eff, bool track) {
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // four partial sums (positions j mod 4), kept as two packed pairs
+        uint64_t ls01 = pk2(0.f, 0.f), ls23 = pk2(0.f, 0.f);
+        const uint64_t cc = pk2(c2, c2), mm = pk2(-m_eff, -m_eff);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t pk[16];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
+          for (int j = 0; j < 32; j += 4) {
             const float s0 = __uint_as_float(sc[c][j]), s1 = __uint_as_float(sc[c][j + 1]);
+            const float s2 = __uint_as_float(sc[c][j + 2]), s3 = __uint_as_float(sc[c][j + 3]);
             if (track) {
-              mx[j & 3] = fmaxf(mx[j & 3], s0);
-              mx[(j + 1) & 3] = fmaxf(mx[(j + 1) & 3], s1);
+              mx[0] = fmaxf(mx[0], s0);
+              mx[1] = fmaxf(mx[1], s1);
+              mx[2] = fmaxf(mx[2], s2);
+              mx[3] = fmaxf(mx[3], s3);
             }
-            const float p0 = ex2(fmaf(s0, c2, -m_eff));
-            const float p1 = ex2(fmaf(s1, c2, -m_eff));
-            ls[j & 3] += p0;
-            ls[(j + 1) & 3] += p1;
+            float x0, x1, x2, x3;
+            upk2(ffma2(pk2(s0, s1), cc, mm), x0, x1);
+            upk2(ffma2(pk2(s2, s3), cc, mm), x2, x3);
+            const float p0 = ex2(x0), p1 = ex2(x1), p2 = ex2(x2), p3 = ex2(x3);
+            ls01 = fadd2(ls01, pk2(p0, p1));
+            ls23 = fadd2(ls23, pk2(p2, p3));
             pk[j / 2] = pack_bf16x2(p0, p1);
+            pk[j / 2 + 1] = pack_bf16x2(p2, p3);
           }
           tst16(p_addr + 16 * c, pk);
         }
-        lsum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        float l0, l1, l2, l3;
+        upk2(ls01, l0, l1);
+        upk2(ls23, l2, l3);
+        lsum = (l0 + l1) + (l2 + l3);
       };
       // before any selected position the weights are taken against 0 (all
       // masked: zeros; otherwise the pass is redone below)
