@@ -508,6 +508,13 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 // lo and hi rounded to bf16 (nearest even), lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
@@ -766,10 +773,8 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
             const float s0 = __uint_as_float(sc[c][j]), s1 = __uint_as_float(sc[c][j + 1]);
             const float s2 = __uint_as_float(sc[c][j + 2]), s3 = __uint_as_float(sc[c][j + 3]);
             if (track) {
-              mx[0] = fmaxf(mx[0], s0);
-              mx[1] = fmaxf(mx[1], s1);
-              mx[2] = fmaxf(mx[2], s2);
-              mx[3] = fmaxf(mx[3], s3);
+              mx[(j >> 2) & 1] = fmax3(mx[(j >> 2) & 1], s0, s1);
+              mx[2 + ((j >> 2) & 1)] = fmax3(mx[2 + ((j >> 2) & 1)], s2, s3);
             }
             float x0, x1, x2, x3;
             upk2(ffma2(pk2(s0, s1), cc, mm), x0, x1);
