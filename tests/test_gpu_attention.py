@@ -172,6 +172,38 @@ def test_graph_replay_follows_new_selections():
     assert np.abs(lg.cpu().numpy() - lse_ref).max() <= 1e-4 + 1e-5 * np.abs(lse_ref).max()
 
 
+def test_no_keys_and_no_tokens():
+    # zero key rows: every selection is empty (o = 0, lse = -inf) and the
+    # key / value pointers are never read; zero tokens: nothing runs
+    torch = _torch()
+    import sparse_attention_indexer_live_gb300 as dsa
+    dev = "cuda:0"
+    T, H, Kc = 20, 16, 32
+    q, _, _, _ = wk.attention_inputs(T, H, 100, Kc, seed=12)
+    qd = torch.from_numpy(q.view(np.int16)).to(dev)
+    kd = torch.empty((0, 128), dtype=torch.int16, device=dev)
+    vd = torch.empty((0, 128), dtype=torch.int16, device=dev)
+    idd = torch.full((T, Kc), -1, dtype=torch.int32, device=dev)
+    cfg = dsa.attention_cfg(qd, kd, idd)
+    ws = torch.full((dsa.dsa_sparse_attention_workspace(cfg),), 0x5A, dtype=torch.uint8, device=dev)
+    o = torch.full((T, H, 128), 7.0, dtype=torch.float32, device=dev)
+    lse = torch.full((T, H), 7.0, dtype=torch.float32, device=dev)
+    dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, 0.1, ws, o, lse)
+    torch.cuda.synchronize()
+    assert dsa.dsa_sparse_attention_status() == dsa.DSA_OK
+    assert torch.all(o == 0) and torch.all(torch.isneginf(lse))
+    q0 = torch.empty((0, H, 128), dtype=torch.int16, device=dev)
+    i0 = torch.empty((0, Kc), dtype=torch.int32, device=dev)
+    cfg0 = dsa.attention_cfg(q0, kd, i0)
+    assert dsa.dsa_sparse_attention_workspace(cfg0) == 0
+    ws0 = torch.empty(0, dtype=torch.uint8, device=dev)
+    o0 = torch.empty((0, H, 128), dtype=torch.float32, device=dev)
+    l0 = torch.empty((0, H), dtype=torch.float32, device=dev)
+    dsa.dsa_sparse_attention(cfg0, q0, kd, vd, i0, 0.1, ws0, o0, l0)
+    torch.cuda.synchronize()
+    assert dsa.dsa_sparse_attention_status() == dsa.DSA_OK
+
+
 def test_unsupported_shapes():
     torch = _torch()
     import sparse_attention_indexer_live_gb300 as dsa
