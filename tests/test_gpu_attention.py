@@ -48,12 +48,14 @@ def _union_from_ws(ws_np, G, Kc, groups):
     return out
 
 
-def _run(T, H, S, Kc, seed, own=0.1, fill=1.0, idx_fn=None, check_union=True):
+def _run(T, H, S, Kc, seed, own=0.1, fill=1.0, idx_fn=None, check_union=True, qk_fn=None, scale=None):
     torch = _torch()
     import sparse_attention_indexer_live_gb300 as dsa
     q, k, v, idx = wk.attention_inputs(T, H, S, Kc, seed=seed, own=own, fill=fill, G=128 // H)
     if idx_fn is not None:
         idx = idx_fn(idx)
+    if qk_fn is not None:
+        q, k = qk_fn(q, k)
     dev = "cuda:0"
     qd, kd, vd, idd = (torch.from_numpy(x.view(np.int16) if x.dtype == np.uint16 else x).to(dev)
                        for x in (q, k, v, idx))
@@ -61,7 +63,7 @@ def _run(T, H, S, Kc, seed, own=0.1, fill=1.0, idx_fn=None, check_union=True):
     ws = torch.zeros(dsa.dsa_sparse_attention_workspace(cfg), dtype=torch.uint8, device=dev)
     o = torch.full((T, H, 128), 7.0, dtype=torch.float32, device=dev)
     lse = torch.full((T, H), 7.0, dtype=torch.float32, device=dev)
-    scale = 1.0 / math.sqrt(128)
+    scale = 1.0 / math.sqrt(128) if scale is None else scale
     dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse)
     torch.cuda.synchronize()
     assert dsa.dsa_sparse_attention_status() == dsa.DSA_OK
@@ -88,6 +90,30 @@ def _run(T, H, S, Kc, seed, own=0.1, fill=1.0, idx_fn=None, check_union=True):
         lerr = np.abs(lg[t] - lse_ref[t])
         assert np.all(lerr <= 1e-4 + 1e-5 * np.abs(lse_ref[t])), f"token {t}: lse error {lerr.max()}"
     return og, lg
+
+
+def _bf16_bits(x):
+    # float32 -> bf16 bit patterns, rounding to nearest even (finite inputs)
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _rising_scores(q, k):
+    # scores that rise with the position: k[j] = 0.55 j / S (+ small noise)
+    # in every dim and q = 0.5 (+ noise), so q . k climbs from about 0 to
+    # about 35 across the key range -- with scale 1 the row maximum rises by
+    # some 50 in base 2 over a group's tiles, far past the threshold at which
+    # the kernel moves its running maximum and rescales the accumulated output
+    S = k.shape[0]
+    rng = np.random.default_rng(5)
+    kf = (0.55 * np.arange(S) / S)[:, None] + 0.05 * rng.standard_normal(k.shape)
+    qf = 0.5 + 0.05 * rng.standard_normal(q.shape)
+    return _bf16_bits(qf), _bf16_bits(kf)
+
+
+def test_running_maximum_rises_across_tiles():
+    # exercises the rescale of O (tile maxima rising by more than 2^8)
+    _run(32, 8, 20000, 512, seed=13, own=0.5, qk_fn=_rising_scores, scale=1.0)
 
 
 def test_union_and_attention_small():
