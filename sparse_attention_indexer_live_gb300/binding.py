@@ -193,29 +193,65 @@ def _stream(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+# Argument checks.  The C ABI sees only pointers, so a tensor of the wrong
+# type, device or size would reach the kernels as an out-of-bounds access;
+# every check below raises (TypeError for a wrong type or dtype, ValueError
+# for a wrong device, layout or size) and none of them is an `assert`, so
+# they stay in force under `python -O`.
+
+def _tensor(name, t, dtypes, *, numel=0, contiguous=True, device=None):
+    """Check one tensor argument: a torch.Tensor of one of `dtypes`, on a CUDA
+    device (`device`, when given, is the required device index), contiguous
+    unless `contiguous` is False, with at least `numel` elements."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if t.dtype not in dtypes:
+        want = " or ".join(str(d) for d in dtypes)
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {want}")
+    if not t.is_cuda:
+        raise ValueError(f"{name}: must be a CUDA tensor (got device {t.device})")
+    if device is not None and t.device.index != device:
+        raise ValueError(f"{name}: on cuda:{t.device.index}, the plan is for cuda:{device}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: {t.numel()} elements, at least {numel} needed")
+    return t
+
+
+def _i32(name, t, numel, device=None):
+    import torch
+    return _tensor(name, t, (torch.int32,), numel=numel, device=device)
+
+
 def _check_tensors(plan: Plan, logits, starts, ends, outs):
     import torch
     c = plan.cfg
-    assert logits.dtype == torch.float32 and logits.is_cuda, "logits: CUDA float32"
+    _tensor("logits", logits, (torch.float32,), contiguous=False, device=plan.device)
     if logits.dim() == 2 and logits.shape[1] == c.width:
-        assert logits.shape[0] == c.rows, "logits rows"
-        assert (c.rows <= 1 or logits.stride(0) == c.row_stride) and \
-            logits.stride(1) == c.col_stride, "logits strides must match the plan"
+        if logits.shape[0] != c.rows:
+            raise ValueError(f"logits: {logits.shape[0]} rows, the plan has {c.rows}")
+        if (c.rows > 1 and logits.stride(0) != c.row_stride) or logits.stride(1) != c.col_stride:
+            raise ValueError(f"logits: strides {tuple(logits.stride())} do not match the plan's "
+                             f"({c.row_stride}, {c.col_stride})")
     else:
         need = (c.rows - 1) * c.row_stride + (c.width - 1) * c.col_stride + 1 if c.rows else 0
-        assert logits.is_contiguous() and logits.numel() >= need, "logits storage too small"
+        if not logits.is_contiguous():
+            raise ValueError("logits: a flat logits buffer must be contiguous")
+        if logits.numel() < need:
+            raise ValueError(f"logits: {logits.numel()} elements, the plan reaches {need}")
     nq = -(-c.rows // c.row_repeat)
-    assert ends.dtype == torch.int32 and ends.is_cuda and ends.is_contiguous() and \
-        ends.numel() >= nq, "ends: CUDA int32 [ceil(rows / row_repeat)]"
+    _i32("ends", ends, nq, plan.device)
     if c.has_starts:
-        assert starts is not None and starts.dtype == torch.int32 and starts.is_cuda and \
-            starts.is_contiguous() and starts.numel() >= nq, "starts"
-    else:
-        assert starts is None, "the plan was made without starts"
+        if starts is None:
+            raise ValueError("starts: the plan was made with starts")
+        _i32("starts", starts, nq, plan.device)
+    elif starts is not None:
+        raise ValueError("starts: the plan was made without starts")
     for name, t, cols in outs:
         if t is not None:
-            assert t.dtype == torch.int32 and t.is_cuda and t.is_contiguous() and \
-                t.numel() >= c.rows * cols, f"{name}: CUDA int32 [rows, {cols}]"
+            _i32(name, t, c.rows * cols, plan.device)
 
 
 def dsa_candidate_select(plan: Plan, logits, starts, ends, cand, stream=None):
@@ -246,18 +282,40 @@ def dsa_select_topk(plan: Plan, logits, starts, ends, cand, topk, stream=None):
 def dsa_combine_window(plan: Plan, starts, ends, topk, window: int, out, stream=None):
     """Union of each row's top-k and the last `window` live columns into
     out [rows, K + window] int32 (ascending, -1 padded)."""
-    import torch
     c = plan.cfg
+    if int(window) < 0:
+        raise ValueError(f"window: {window} is negative")
     nq = -(-c.rows // c.row_repeat)
-    assert ends.dtype == torch.int32 and ends.is_cuda and ends.numel() >= nq, "ends"
-    assert (starts is None) == (not c.has_starts), "starts"
-    assert topk.dtype == torch.int32 and topk.is_cuda and topk.is_contiguous() and \
-        topk.numel() >= c.rows * c.row_topk, "topk"
-    assert out.dtype == torch.int32 and out.is_cuda and out.is_contiguous() and \
-        out.numel() >= c.rows * (c.row_topk + window), "out: CUDA int32 [rows, K + window]"
+    _i32("ends", ends, nq, plan.device)
+    if c.has_starts:
+        if starts is None:
+            raise ValueError("starts: the plan was made with starts")
+        _i32("starts", starts, nq, plan.device)
+    elif starts is not None:
+        raise ValueError("starts: the plan was made without starts")
+    _i32("topk", topk, c.rows * c.row_topk, plan.device)
+    _i32("out", out, c.rows * (c.row_topk + int(window)), plan.device)
     _check(load().dsa_combine_window(plan.handle, _ptr(starts), _ptr(ends), _ptr(topk),
                                      int(window), _ptr(out), _stream(stream)),
            "dsa_combine_window")
+
+
+def _indexer_args(q, k, k_scale, w, ends, device=None):
+    """Check the producer's inputs; returns (T, H, D, S)."""
+    import torch
+    _tensor("q", q, (torch.uint8,), device=device)
+    if q.dim() != 3:
+        raise ValueError(f"q: shape {tuple(q.shape)}, expected [queries, heads, head_dim]")
+    T, H, D = q.shape
+    dev = q.device.index
+    _tensor("k", k, (torch.uint8,), device=dev)
+    if k.dim() != 2 or k.shape[1] != D:
+        raise ValueError(f"k: shape {tuple(k.shape)}, expected [keys, {D}] (q's head_dim)")
+    S = k.shape[0]
+    _tensor("k_scale", k_scale, (torch.float32,), numel=S, device=dev)
+    _tensor("w", w, (torch.float32,), numel=T * H, device=dev)
+    _i32("ends", ends, T, dev)
+    return T, H, D, S
 
 
 def dsa_indexer_logits(q, k, k_scale, w, starts, ends, logits, stream=None):
@@ -265,14 +323,14 @@ def dsa_indexer_logits(q, k, k_scale, w, starts, ends, logits, stream=None):
     uint8 e4m3 bytes, k_scale [S] f32, w [T, 64] f32, bounds [T] int32,
     logits [T, ld] f32 written over each query's live span."""
     import torch
-    T, H, D = q.shape
-    S = k.shape[0]
-    for name, t, dt in (("q", q, torch.uint8), ("k", k, torch.uint8), ("k_scale", k_scale,
-                        torch.float32), ("w", w, torch.float32), ("ends", ends, torch.int32)):
-        assert t.dtype == dt and t.is_cuda and t.is_contiguous(), name
-    assert starts is None or (starts.dtype == torch.int32 and starts.is_cuda)
-    assert logits.dtype == torch.float32 and logits.is_cuda and logits.dim() == 2 and \
-        logits.stride(1) == 1 and logits.shape[0] == T and logits.shape[1] >= S
+    T, H, D, S = _indexer_args(q, k, k_scale, w, ends)
+    dev = q.device.index
+    if starts is not None:
+        _i32("starts", starts, T, dev)
+    _tensor("logits", logits, (torch.float32,), contiguous=False, device=dev)
+    if logits.dim() != 2 or logits.stride(1) != 1 or logits.shape[0] != T or logits.shape[1] < S:
+        raise ValueError(f"logits: shape {tuple(logits.shape)} strides {tuple(logits.stride())}, "
+                         f"expected [{T}, >= {S}] with unit column stride")
     cfg = dsa_indexer_cfg(queries=T, keys=S, heads=H, head_dim=D, out_stride=logits.stride(0))
     _check(load().dsa_indexer_logits(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(k_scale), _ptr(w),
                                      _ptr(starts), _ptr(ends), _ptr(logits), _stream(stream)),
@@ -287,23 +345,24 @@ def dsa_indexer_select_workspace(plan: Plan) -> int:
     return int(n.value)
 
 
+def _fused_args(plan: Plan, q, k, k_scale, w, ends, cand, topk):
+    T, H, D, S = _indexer_args(q, k, k_scale, w, ends, plan.device)
+    c = plan.cfg
+    if T != c.rows or S != c.width:
+        raise ValueError(f"q / k: {T} queries x {S} keys, the plan is {c.rows} rows x {c.width}")
+    _i32("cand", cand, c.rows * (c.block_topk + 1), plan.device)
+    _i32("topk", topk, c.rows * c.row_topk, plan.device)
+    return dsa_indexer_cfg(queries=T, keys=S, heads=H, head_dim=D, out_stride=S)
+
+
 def dsa_indexer_select(plan: Plan, q, k, k_scale, w, ends, workspace, cand, topk, stream=None):
     """The indexer logits fused with the selection (never materialised):
     q [T, 64, 128] and k [S, 128] uint8 e4m3 bytes, k_scale [S] f32, w [T, 64]
     f32, ends [T] int32; workspace a CUDA uint8 tensor of at least
     dsa_indexer_select_workspace(plan) bytes; cand [T, Kb + 1], topk [T, K]."""
     import torch
-    T, H, D = q.shape
-    S = k.shape[0]
-    for name, t, dt in (("q", q, torch.uint8), ("k", k, torch.uint8), ("k_scale", k_scale,
-                        torch.float32), ("w", w, torch.float32), ("ends", ends, torch.int32),
-                        ("workspace", workspace, torch.uint8)):
-        assert t.dtype == dt and t.is_cuda and t.is_contiguous(), name
-    c = plan.cfg
-    for name, t, cols in (("cand", cand, c.block_topk + 1), ("topk", topk, c.row_topk)):
-        assert t.dtype == torch.int32 and t.is_cuda and t.is_contiguous() and \
-            t.numel() >= c.rows * cols, f"{name}: CUDA int32 [rows, {cols}]"
-    cfg = dsa_indexer_cfg(queries=T, keys=S, heads=H, head_dim=D, out_stride=S)
+    cfg = _fused_args(plan, q, k, k_scale, w, ends, cand, topk)
+    _tensor("workspace", workspace, (torch.uint8,), device=plan.device)
     _check(load().dsa_indexer_select(plan.handle, ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(k_scale),
                                      _ptr(w), _ptr(ends), _ptr(workspace), workspace.numel(),
                                      _ptr(cand), _ptr(topk), _stream(stream)),
@@ -319,17 +378,7 @@ def dsa_indexer_select_noalloc(plan: Plan, q, k, k_scale, w, ends, cand, topk, s
     (dsa_indexer_select_workspace) exceeds that array are refused.  All calls
     on a device share the array: keep them ordered (one stream), and make the
     first call on a device before any stream capture."""
-    import torch
-    T, H, D = q.shape
-    S = k.shape[0]
-    for name, t, dt in (("q", q, torch.uint8), ("k", k, torch.uint8), ("k_scale", k_scale,
-                        torch.float32), ("w", w, torch.float32), ("ends", ends, torch.int32)):
-        assert t.dtype == dt and t.is_cuda and t.is_contiguous(), name
-    c = plan.cfg
-    for name, t, cols in (("cand", cand, c.block_topk + 1), ("topk", topk, c.row_topk)):
-        assert t.dtype == torch.int32 and t.is_cuda and t.is_contiguous() and \
-            t.numel() >= c.rows * cols, f"{name}: CUDA int32 [rows, {cols}]"
-    cfg = dsa_indexer_cfg(queries=T, keys=S, heads=H, head_dim=D, out_stride=S)
+    cfg = _fused_args(plan, q, k, k_scale, w, ends, cand, topk)
     _check(load().dsa_indexer_select_noalloc(plan.handle, ctypes.byref(cfg), _ptr(q), _ptr(k),
                                              _ptr(k_scale), _ptr(w), _ptr(ends), _ptr(cand),
                                              _ptr(topk), _stream(stream)),
@@ -349,12 +398,16 @@ def dsa_sparse_attention_workspace(cfg: dsa_attention_cfg) -> int:
     return int(n.value)
 
 
+def _attention_idx(cfg: dsa_attention_cfg, idx, workspace):
+    import torch
+    _i32("idx", idx, max(cfg.tokens, 0) * max(cfg.select, 0))
+    _tensor("workspace", workspace, (torch.uint8,), device=idx.device.index)
+
+
 def dsa_group_union(cfg: dsa_attention_cfg, idx, workspace, stream=None):
     """The unions of each group's selections and their token masks, written
     to workspace (layout in include/dsa_select.h)."""
-    import torch
-    assert idx.dtype == torch.int32 and idx.is_cuda and idx.is_contiguous(), "idx"
-    assert workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace"
+    _attention_idx(cfg, idx, workspace)
     _check(load().dsa_group_union(ctypes.byref(cfg), _ptr(idx), _ptr(workspace), workspace.numel(),
                                   _stream(stream)), "dsa_group_union")
 
@@ -365,13 +418,16 @@ def dsa_sparse_attention(cfg: dsa_attention_cfg, q, k, v, idx, scale: float, wor
     tensors (or their uint16 bit patterns), idx [T, Kc] int32; writes o
     [T, H, 128] and lse [T, H] (float32)."""
     import torch
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        assert t.dtype in (torch.bfloat16, torch.uint16, torch.int16) and t.is_cuda and \
-            t.is_contiguous(), name
-    assert idx.dtype == torch.int32 and idx.is_cuda and idx.is_contiguous(), "idx"
-    for name, t in (("o", o), ("lse", lse)):
-        assert t.dtype == torch.float32 and t.is_cuda and t.is_contiguous(), name
-    assert workspace.dtype == torch.uint8 and workspace.is_cuda, "workspace"
+    _attention_idx(cfg, idx, workspace)
+    dev = idx.device.index
+    T, H, S = max(cfg.tokens, 0), max(cfg.heads, 0), max(cfg.keys, 0)
+    D, Dv = max(cfg.head_dim, 0), max(cfg.value_dim, 0)
+    half = (torch.bfloat16, torch.uint16, torch.int16)
+    _tensor("q", q, half, numel=T * H * D, device=dev)
+    _tensor("k", k, half, numel=S * D, device=dev)
+    _tensor("v", v, half, numel=S * Dv, device=dev)
+    _tensor("o", o, (torch.float32,), numel=T * H * Dv, device=dev)
+    _tensor("lse", lse, (torch.float32,), numel=T * H, device=dev)
     _check(load().dsa_sparse_attention(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx),
                                        float(scale), _ptr(workspace), workspace.numel(), _ptr(o),
                                        _ptr(lse), _stream(stream)), "dsa_sparse_attention")

@@ -184,11 +184,22 @@ def test_unsupported_and_invalid():
     with pytest.raises(dsa.DsaSelectError) as e:
         dsa.dsa_indexer_select(plan, qd, kd, ksd, wd, end, small, cand, topk)
     assert e.value.status == dsa.DSA_ERR_INVALID_ARG
-    # the plan's width must be the key count
+    # the plan's width must be the key count: the binding refuses it on the
+    # host, and so does the C ABI when called directly
     other = dsa.dsa_select_init(rows=T, width=S + 1, block_size=8, block_topk=32, row_topk=64)
     ws = torch.empty(dsa.dsa_indexer_select_workspace(other), dtype=torch.uint8, device=dev)
-    with pytest.raises(dsa.DsaSelectError) as e:
+    with pytest.raises(ValueError):
         dsa.dsa_indexer_select(other, qd, kd, ksd, wd, end, ws, cand, topk)
-    assert e.value.status == dsa.DSA_ERR_INVALID_ARG
+    import ctypes
+    from sparse_attention_indexer_live_gb300 import binding
+    icfg = binding.dsa_indexer_cfg(queries=T, keys=S, heads=64, head_dim=128, out_stride=S)
+    ptr = binding._ptr
+    st = dsa.load().dsa_indexer_select(other.handle, ctypes.byref(icfg), ptr(qd), ptr(kd), ptr(ksd),
+                                       ptr(wd), ptr(end), ptr(ws), ws.numel(), ptr(cand), ptr(topk),
+                                       binding._stream(None))
+    assert st == dsa.DSA_ERR_INVALID_ARG
+    # undersized outputs never reach the library
+    with pytest.raises(ValueError):
+        dsa.dsa_indexer_select(plan, qd, kd, ksd, wd, end, ws, cand[:3], topk)
     torch.cuda.synchronize()
     assert dsa.dsa_indexer_status() == dsa.DSA_OK
