@@ -307,11 +307,14 @@ int dsa_sparse_attention_status(void);
  *   Limit: the array holds DSA_NOALLOC_SCRATCH_BYTES (8 MiB) on every device
  *   that loads the library, until the process exits.  A plan whose
  *   dsa_indexer_select_workspace() exceeds it gets DSA_ERR_UNSUPPORTED (at
- *   block size 8 and Kb 256: about 110 queries of 131,072 keys, 16 of
+ *   block size 8 and Kb 256: 112 queries of 131,072 keys, 15 of
  *   1,048,576).
  *   Set-up: the first call on a device looks up the array's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture begins.
+ *   before any stream capture begins.  The address is kept with the id of
+ *   the context it belongs to; after a device reset the next call sees a new
+ *   context and looks the address up again (that call, too, belongs before
+ *   any capture).
  *   Sharing: every call on a device uses the same array, and each call
  *   overwrites what the last one left there (nothing in it has to start at
  *   zero: a call writes every part of it that it reads back).  Calls that can

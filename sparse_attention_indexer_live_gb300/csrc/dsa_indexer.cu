@@ -744,17 +744,55 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
 // The allocation-free variant's records: one fixed array per device, in the
 // module, so the call never allocates.  Host code must not pass the array's
 // name to a kernel (on the host it is only a stand-in for the symbol); the
-// device address comes from cudaGetSymbolAddress, looked up once per device.
+// device address comes from cudaGetSymbolAddress, taken with the device
+// current.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[DSA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
 constexpr int kNoallocMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kNoallocMaxDevices];
 
-// The array's device address on the current device; the first request on a
-// device looks it up with that device current.
+// The address is kept per device together with the unique id of the context
+// it was taken in.  A device reset (or any teardown of the primary context)
+// reloads the module in a new context with a new id, so a stale address is
+// never reused: a changed id, or no id at all, means look it up again.
+struct NoallocSlot {
+  void* ptr;
+  unsigned long long ctx_id;
+  bool have_id;
+};
+NoallocSlot g_noalloc_slot[kNoallocMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <typename Fn>
+Fn driver_fn(const char* name) {
+  void* ptr = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &ptr, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return reinterpret_cast<Fn>(ptr);
+}
+
+// The unique id of the calling thread's current context; false when there
+// is none yet or the driver does not provide the query.
+bool current_ctx_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_cur = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  if (!get_cur || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS || !ctx) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// The array's device address on the current device.  The first request on a
+// device -- and the first after its context was replaced -- looks it up with
+// that device current.
 int noalloc_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -763,15 +801,21 @@ int noalloc_scratch(void** out) {
   }
   if (dev < 0 || dev >= kNoallocMaxDevices) return DSA_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  NoallocSlot& sl = g_noalloc_slot[dev];
+  unsigned long long id = 0;
+  const bool have = current_ctx_id(&id);
+  if (!sl.ptr || !have || !sl.have_id || sl.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
       cudaGetLastError();
+      sl.ptr = nullptr;
       return DSA_ERR_CUDA;
     }
-    g_noalloc_ptr[dev] = p;
+    sl.ptr = p;
+    // the lookup makes the runtime's context current if it was not yet
+    sl.have_id = current_ctx_id(&sl.ctx_id);
   }
-  *out = g_noalloc_ptr[dev];
+  *out = sl.ptr;
   return DSA_OK;
 }
 
