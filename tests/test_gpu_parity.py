@@ -177,10 +177,7 @@ def test_ragged_workload_full():
 def test_decode_1m_workload_full():
     wl = wk.WORKLOADS["decode_1m"]
     x, s, e = wk.make_all(wl)
-    case = Case.from_workload(wl, x, s, e)
-    want_logits, want_cand, want_topk = case.oracle()
-    run = DeviceRun(case).fused()
-    assert_run_matches(run, want_logits, want_cand, want_topk, "decode_1m [fused]")
+    check_all_modes(Case.from_workload(wl, x, s, e), what="decode_1m")
 
 
 def test_row_repeat_shared_end_reading():

@@ -296,6 +296,40 @@ def indexer_inputs(T: int, S: int, seed: int = 7, heads: int = 64, dim: int = 12
     return q, k, ks, w, None, ends
 
 
+# OCP E4M3 bytes of small integers (value = 2^(e - 7) * (1 + m / 8)):
+# 1 = e 7, 2 = e 8, 3 = e 8 with m 4; bit 7 is the sign.
+E4M3_INT = {1: 0x38, 2: 0x40, 3: 0x44, -1: 0xB8, -2: 0xC0, -3: 0xC4}
+_S_XQ = 131
+_S_XK = 132
+_S_XPOOL = 133
+_S_XW = 134
+_S_XKS = 135
+
+
+def indexer_exact_inputs(T: int, S: int, seed: int = 3, heads: int = 64, dim: int = 128,
+                         pool: int = 48):
+    """(q, k, k_scale, w, starts, ends) whose indexer logits are exact in fp32.
+
+    q holds e4m3 integers in {+-1, +-2, +-3}, k in {+-1, +-2}: every product is
+    an integer and a head's dot product stays within 128 * 6 = 768.  The head
+    weights are powers of two in [1/4, 2] (positive, so no head sum is -0) and
+    the key scales powers of two in [1/2, 2] (half of them 1): the weighted
+    head sum is a multiple of 1/4 below 2^17, so every partial sum is
+    representable in fp32 whatever the order.  Keys are drawn from a pool of
+    `pool` distinct rows, so equal logits (ties) are common.  Causal ends."""
+    qv = np.array([1, 2, 3, -1, -2, -3])
+    kv = np.array([1, 2, -1, -2])
+    enc = np.vectorize(E4M3_INT.get, otypes=[np.uint8])
+    q = enc(qv[u32(seed, _S_XQ, 0, T * heads * dim) % 6]).reshape(T, heads, dim)
+    rows = enc(kv[u32(seed, _S_XK, 0, pool * dim) % 4]).reshape(pool, dim)
+    k = np.ascontiguousarray(rows[u32(seed, _S_XPOOL, 0, S) % pool])
+    w = (2.0 ** (u32(seed, _S_XW, 0, T * heads) % 4 - 2.0)).astype(np.float32).reshape(T, heads)
+    e = u32(seed, _S_XKS, 0, S) % 4
+    ks = (2.0 ** np.where(e == 3, 0, e.astype(np.int64) - 1)).astype(np.float32)
+    ends = (S - T + 1 + np.arange(T)).clip(0, S).astype(np.int32)
+    return q, k, ks, w, None, ends
+
+
 # ---------------------------------------------------------------------------
 # grouped sparse attention inputs
 
