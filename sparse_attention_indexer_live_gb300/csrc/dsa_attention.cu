@@ -553,7 +553,11 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
 
   if (threadIdx.x == 0) {
     s_attn_abort = 0;
+#ifdef DSA_ATTENTION_TEST_STARVE
+    bar_init(qfull, 65);  // test builds only: one arrival more than the Q copy makes, so the waits run out
+#else
     bar_init(qfull, 64);
+#endif
     for (int i = 0; i < kVStages; ++i) {
       bar_init(&vfull[i], 32);
       bar_init(&vempty[i], 1);
