@@ -30,8 +30,8 @@
  *        is set), the (nblocks + 1)-byte flag row with the edge flag in the
  *        last slot, bounds indexed by row // ROW_REPEAT.
  *
- * Readings where the pages are silent (each is fixed here and listed in the
- * design notes):
+ * Readings where the pages are silent (each one a choice this oracle fixes,
+ * and the GPU path follows the same choice):
  *   - order: IEEE-754 totalOrder on the fp32 bits (-NaN < -inf < ... < -0 <
  *     +0 < ... < +inf < +NaN); "better" = larger, equal keys -> lower index;
  *   - block score = max over the block's live columns (partial last block
@@ -372,7 +372,7 @@ int oracle_indexer_logits(const uint8_t* q, const uint8_t* k, const float* k_sca
  * runs over the union of the group's selected KV positions, and the result
  * stays query-exact (each token attends to its own selection only).  The
  * pages fix neither the attention's dimensions nor its formula; the readings
- * taken (listed in the design notes): multi-query attention in which a
+ * this oracle takes: multi-query attention in which a
  * token's H heads share the selected key/value rows, scores scale * q . k,
  * softmax over the token's selection, the log-sum-exp in natural log; an
  * empty selection gives o = 0 and lse = -inf.
