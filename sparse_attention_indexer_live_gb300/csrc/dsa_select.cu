@@ -81,6 +81,7 @@ struct Params {
   int32_t scan_prm;
   int32_t epoch;         // streaming rounds between two capacity checks (128-bit path)
   int32_t scan_epoch;    // the same for the scan-mode buffer
+  int32_t small_cap;     // candidate entries of the short-row path (0: path off)
 };
 
 // Scratch with a fixed size, in static shared memory.
@@ -749,6 +750,403 @@ __device__ void row_topk_kept(const Params& p, Src& src, const Row& R, int r, co
 }
 
 // ---------------------------------------------------------------------------
+// Short rows (the decode case): a live span of at most one streaming round
+// (kSmallCols columns) is read once into registers.  Only the warps that hold
+// part of the span stay after the first barrier (the others exit) and they
+// synchronise among themselves on a named barrier, so a short row costs
+// issue slots in proportion to its length.  Block maxima come from shuffles;
+// the block top-k and the row top-k compact their candidates into shared
+// memory and radix-select them (one barrier per 8-bit digit); the mask is
+// written from registers; cand and topk are emitted in index order by
+// prefixes.  The result is exactly the general path's; a row this path does
+// not cover (a block whose maximum is -NaN, which ranks below the -inf padding
+// blocks) goes to the general path.
+
+constexpr int kSmallCols = kThreads * kVecPerThread * 4;  // 8192 columns
+constexpr int kChunks = kWarps * kVecPerThread;           // 64 chunks of 32 vectors
+static_assert(kChunks == 64, "chunk_offsets scans 64 chunk totals with one warp");
+
+// Scratch of the short-row path at the start of the dynamic shared memory,
+// followed by the candidate array.
+struct SmallScratch {
+  uint32_t hist[3][256];      // rotating radix histograms
+  int32_t chunk[2][kChunks];  // chunk totals of two successive index-order prefixes
+};
+static_assert(sizeof(SmallScratch) % 16 == 0, "the candidate array follows 16-byte aligned");
+
+// Barrier of the first n threads (whole warps) of the CTA; the other warps
+// have exited.
+__device__ __forceinline__ void live_sync(int n) { asm volatile("bar.sync 1, %0;" ::"r"(n) : "memory"); }
+
+// Radix select over the n distinct composites a[0 .. n) in shared memory, by
+// the first `nt` threads: returns X with exactly k entries >= X
+// (1 <= k <= n).  8-bit digits from the top, stopping once the threshold
+// digit's bucket is taken whole.  The histograms rotate over three buffers,
+// so a digit costs one barrier: in pass p the buffer of pass p + 1 is cleared
+// (its last readers finished before the barrier of pass p - 1 ended), and
+// every warp reads the histogram of pass p after its barrier and finds the
+// digit itself.  hist[hb] must be zero on entry; on return hb names a buffer
+// that is zero and no longer read.
+__device__ uint64_t smem_select(const uint64_t* a, int n, int k, SmallScratch& ss, int& hb, int nt) {
+  const int lane = threadIdx.x & 31;
+  uint64_t prefix = 0, mask = 0;
+  uint32_t kk = (uint32_t)k;
+  int b = hb;
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    uint32_t* h = ss.hist[b];
+    const int nbuf = b == 2 ? 0 : b + 1;
+    for (int i = threadIdx.x; i < 256; i += nt) ss.hist[nbuf][i] = 0u;
+    for (int i = threadIdx.x; i < n; i += nt) {
+      const uint64_t c = a[i];
+      if ((c & mask) == prefix) atomicAdd(&h[(uint32_t)(c >> shift) & 0xFFu], 1u);
+    }
+    live_sync(nt);
+    uint32_t hv[8];
+    uint32_t tot = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      hv[q] = h[8 * lane + q];
+      tot += hv[q];
+    }
+    uint32_t incl = tot;  // entries in this lane's bins and every higher lane's
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_down_sync(kFull, incl, o);
+      if (lane + o < 32) incl += y;
+    }
+    uint32_t cum = incl - tot;
+    uint32_t found = 0, d = 0, above = 0, cntd = 0;
+#pragma unroll
+    for (int q = 7; q >= 0; --q) {
+      if (!found && cum < kk && cum + hv[q] >= kk) {
+        found = 1;
+        d = (uint32_t)(8 * lane + q);
+        above = cum;
+        cntd = hv[q];
+      }
+      cum += hv[q];
+    }
+    const int src = __ffs(__ballot_sync(kFull, found)) - 1;
+    d = __shfl_sync(kFull, d, src & 31);
+    above = __shfl_sync(kFull, above, src & 31);
+    cntd = __shfl_sync(kFull, cntd, src & 31);
+    kk -= above;
+    prefix |= (uint64_t)d << shift;
+    mask |= (uint64_t)0xFFu << shift;
+    b = nbuf;
+    if (cntd == kk) break;
+  }
+  hb = b;
+  return prefix;
+}
+
+// Positions in index order: this thread's counts cnt[u] for its vectors
+// v = (warp * kVecPerThread + u) * 32 + lane become exclusive offsets over the
+// first nw warps' vectors in v order.  One barrier of those warps; `chunk`
+// (kChunks entries) must not be read by anyone when called.
+__device__ void chunk_offsets(const int (&cnt)[kVecPerThread], int (&off)[kVecPerThread], int32_t* chunk,
+                              int nw) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nch = nw * kVecPerThread;
+  int incl[kVecPerThread];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    int x = cnt[u];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    incl[u] = x;
+    if (lane == 31) chunk[warp * kVecPerThread + u] = x;
+  }
+  live_sync(nw * 32);
+  int a = lane < nch ? chunk[lane] : 0, c = 32 + lane < nch ? chunk[32 + lane] : 0;
+  const int a0 = a, c0 = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(kFull, a, o);
+    const int z = __shfl_up_sync(kFull, c, o);
+    if (lane >= o) {
+      a += y;
+      c += z;
+    }
+  }
+  const int tot_a = __shfl_sync(kFull, a, 31);
+  const int ex_a = a - a0, ex_c = tot_a + c - c0;  // exclusive offsets of chunks lane, 32 + lane
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int ci = warp * kVecPerThread + u;
+    const int ea = __shfl_sync(kFull, ex_a, ci & 31);
+    const int ec = __shfl_sync(kFull, ex_c, ci & 31);
+    off[u] = (ci < 32 ? ea : ec) + incl[u] - cnt[u];
+  }
+}
+
+// The whole path for one row whose live span is at most kSmallCols columns
+// on the 128-bit path, with room for its candidates and keys (p.small_cap
+// entries after the scratch).  Returns false, having written nothing but (for
+// L <= K) the row top-k the general path writes too, when a live block's
+// maximum is -NaN: the general path then takes the row.  All threads call;
+// the return value is uniform.  On true, warps past the span may have left
+// before the others finish.
+template <bool kTopK>
+__device__ __noinline__ bool small_row(const Params& p, float* rowp, const Row& R, int r, uint8_t* dyn) {
+  SmallScratch& ss = *reinterpret_cast<SmallScratch*>(dyn);
+  uint64_t* arr = reinterpret_cast<uint64_t*>(dyn + sizeof(SmallScratch));
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g_log2 = p.vec_log2g, g = 1 << g_log2;
+  const int32_t L = R.L, nb = R.nb;
+  const int64_t s = R.s, W = p.width;
+  const int Kb = p.Kb, K = p.K;
+  const int32_t nv = (L + 3) >> 2, nv_full = L >> 2;
+  const float ninf = __uint_as_float(kNegInfBits);
+  const float filler = __uint_as_float(kFillerBits);
+  // warps that hold part of the span (at least one: the row's outputs)
+  const int nw = max(1, (nv + kVecPerThread * 32 - 1) / (kVecPerThread * 32));
+  const bool live = warp < nw;
+  if (threadIdx.x < 256) ss.hist[0][threadIdx.x] = 0u;
+  // 1. the span, one 16-byte vector per (u, thread)
+  float4 x[kVecPerThread];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const int32_t v = (warp * kVecPerThread + u) * 32 + lane;
+    x[u] = make_float4(filler, filler, filler, filler);
+    if (v < nv_full) {
+      x[u] = __ldcs(reinterpret_cast<const float4*>(rowp + s) + v);
+    } else if (v < nv) {  // the span's last, partial vector
+      const float* sp = rowp + s + 4 * (int64_t)v;
+      const int rem = L - 4 * v;
+      x[u].x = sp[0];
+      if (rem > 1) x[u].y = sp[1];
+      if (rem > 2) x[u].z = sp[2];
+    }
+  }
+  int32_t* out = kTopK ? p.topk + (int64_t)r * K : nullptr;
+  if (kTopK && L <= K)  // the span itself, whatever the values
+    for (int i = threadIdx.x; i < K; i += kThreads) out[i] = i < L ? (int32_t)(s + i) : -1;
+  // 2. block maxima; the block's first lane holds its maximum's key
+  // (composite with the block id: bcomp)
+  uint32_t bm[kVecPerThread];
+  bool nan_block = false;
+  if (live) {
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+      uint32_t m = max4key(x[u]);
+      for (int o = 1; o < g; o <<= 1) m = max(m, __shfl_xor_sync(kFull, m, o));
+      const int32_t j = ((warp * kVecPerThread + u) * 32 + lane) >> g_log2;
+      const bool lead = (lane & (g - 1)) == 0 && j < nb;
+      bm[u] = lead ? m : 0u;
+      nan_block |= lead && m < kKeyNegInf;
+    }
+  }
+  auto bcomp = [&](int u) -> uint64_t {
+    const int32_t j = ((warp * kVecPerThread + u) * 32 + lane) >> g_log2;
+    return ((lane & (g - 1)) == 0 && j < nb) ? compose(bm[u], (uint32_t)j) : 0;
+  };
+  // the row top-k reads the span's keys from shared memory, in column order
+  // after the candidate array; the mask below updates them
+  const bool row_sel = kTopK && L > K;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(
+      reinterpret_cast<uint8_t*>(arr) + (((size_t)p.small_cap * 8 - (size_t)L * 4) & ~(size_t)15));
+  if (row_sel && live) {
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const int32_t v = (warp * kVecPerThread + u) * 32 + lane;
+      if (v < nv_full) {
+        *reinterpret_cast<uint4*>(keys + 4 * v) =
+            make_uint4(order_key(__float_as_uint(x[u].x)), order_key(__float_as_uint(x[u].y)),
+                       order_key(__float_as_uint(x[u].z)), order_key(__float_as_uint(x[u].w)));
+      } else if (v < nv) {
+        const int rem = L - 4 * v;
+        keys[4 * v] = order_key(__float_as_uint(x[u].x));
+        if (rem > 1) keys[4 * v + 1] = order_key(__float_as_uint(x[u].y));
+        if (rem > 2) keys[4 * v + 2] = order_key(__float_as_uint(x[u].z));
+      }
+    }
+  }
+  if (__syncthreads_or(nan_block)) return false;
+  // From here on the first nw2 warps continue, on barrier 1: the warps that
+  // hold the span, or all of them when the row top-k is taken (it spreads the
+  // span over every warp); the others exit.
+  const int nw2 = row_sel ? kWarps : nw;
+  const int nt = nw2 * 32;
+  if (warp >= nw2) return true;
+  // 3. block top-k: every live block when they are at most Kb, else the best Kb
+  int hb = 0;
+  uint64_t Xb = 0;
+  int cnt[kVecPerThread], off[kVecPerThread];
+  if (nb > Kb) {
+    // the live blocks' composites in id order, then the Kb-th best of them
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) cnt[u] = live && bcomp(u) != 0;
+    chunk_offsets(cnt, off, ss.chunk[0], nw2);
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u)
+      if (cnt[u]) arr[off[u]] = bcomp(u);
+    live_sync(nt);
+    Xb = smem_select(arr, nb, Kb, ss, hb, nt);
+  }
+  int32_t* crow = p.cand + (int64_t)r * (Kb + 1);
+  // the pin: B is a power of two on this path (and e - 1 - s >= 0 here)
+  const int64_t pin = R.e > s ? (R.e - 1 - s) >> p.log2B : -1;
+  const bool pin_inside = pin >= 0 && s + (pin << p.log2B) < W;
+  const bool edge = pin >= 0 && !pin_inside;  // the chosen blocks of this path all lie inside W
+  bool chosen[kVecPerThread];
+#pragma unroll
+  for (int u = 0; u < kVecPerThread; ++u) {
+    const uint64_t c = live ? bcomp(u) : 0;
+    chosen[u] = c != 0 && c >= Xb;
+    cnt[u] = chosen[u] ? 1 : 0;
+  }
+  if (nb > Kb) {
+    chunk_offsets(cnt, off, ss.chunk[1], nw2);
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u)
+      if (chosen[u] && off[u] < Kb) crow[off[u]] = ((warp * kVecPerThread + u) * 32 + lane) >> g_log2;
+  } else {
+    // every live block, then the -inf padding blocks nb, nb + 1, ... by id
+    const int take = (int)(p.nblocks < Kb ? p.nblocks : Kb);
+    for (int i = threadIdx.x; i < Kb; i += nt) crow[i] = i < take ? i : -1;
+  }
+  if (threadIdx.x == 0) crow[Kb] = (int32_t)pin;
+  // 4. mask: [0, min(s, ecm)) entirely, then the columns of blocks not kept
+  // (their keys become -inf's for the row top-k)
+  const int64_t P = s < (int64_t)R.ecm ? s : (int64_t)R.ecm;
+  for (int64_t c = threadIdx.x; c < P; c += nt) rowp[c] = ninf;
+  const bool edge_keep = edge && (W - 1) < R.ecm && (W - 1) >= s;
+  const float4 ninf4 = make_float4(ninf, ninf, ninf, ninf);
+  if (nb > Kb && live) {
+#pragma unroll
+    for (int u = 0; u < kVecPerThread; ++u) {
+      const int32_t v = (warp * kVecPerThread + u) * 32 + lane;
+      const int32_t j = v >> g_log2;
+      bool kept = __shfl_sync(kFull, chosen[u], lane & ~(g - 1));
+      kept = kept || (pin_inside && j == pin);
+      if (v < nv && !kept) {
+        const int64_t c0 = s + 4 * (int64_t)v;
+        if (v < nv_full && !(edge_keep && c0 + 3 >= W - 1 && c0 <= W - 1)) {
+          __stcs(reinterpret_cast<float4*>(rowp + c0), ninf4);
+          if (row_sel)
+            *reinterpret_cast<uint4*>(keys + 4 * v) = make_uint4(kKeyNegInf, kKeyNegInf, kKeyNegInf, kKeyNegInf);
+        } else {
+          // the span's last, partial vector, or the one holding the kept edge column
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int64_t c = c0 + q;
+            if (c < s + L && !(edge_keep && c == W - 1)) {
+              rowp[c] = ninf;
+              if (row_sel) keys[4 * v + q] = kKeyNegInf;
+            }
+          }
+        }
+      }
+    }
+  }
+  if (!row_sel) return true;
+  // 5. row top-k: the best K columns of the masked span by (value, column),
+  // taken tier by tier -- values above -inf (kept columns), then -inf (every
+  // masked column, and kept -inf values), then below (-NaN) -- so the radix
+  // select runs only over the tier that holds the K-th.  Every warp owns a
+  // contiguous run of 32-column chunks (lane l: column l of a chunk), so
+  // shared-memory reads and the output stores are coalesced and positions in
+  // column order come from ballots and one prefix over the warps.
+  live_sync(nt);
+  const int nck = (L + 31) >> 5;
+  const int cpw = (nck + kWarps - 1) / kWarps;
+  const int c_lo = min(warp * cpw, nck), c_hi = min(c_lo + cpw, nck);
+  const uint32_t lt = lanemask_lt();
+  auto key_at = [&](int col) { return col < L ? keys[col] : 0u; };
+  int whi = 0, weq = 0, wlo = 0;
+  for (int c = c_lo; c < c_hi; ++c) {
+    const int col = 32 * c + lane;
+    const uint32_t kq = key_at(col);
+    whi += __popc(__ballot_sync(kFull, kq > kKeyNegInf));
+    weq += __popc(__ballot_sync(kFull, kq == kKeyNegInf));
+    wlo += __popc(__ballot_sync(kFull, col < L && kq < kKeyNegInf));
+  }
+  int32_t* wt = ss.chunk[0];  // [0, 16): above -inf, [16, 32): -inf, [32, 48): below, [48, 64): picked
+  if (lane == 0) {
+    wt[warp] = whi;
+    wt[16 + warp] = weq;
+    wt[32 + warp] = wlo;
+  }
+  live_sync(nt);
+  // exclusive prefixes over the warps (lane w of the scan is warp w) and totals
+  auto warp_prefix = [&](int base, int& total) {
+    int x = lane < kWarps ? wt[base + lane] : 0;
+    const int x0 = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(kFull, x, o);
+      if (lane >= o) x += y;
+    }
+    total = __shfl_sync(kFull, x, 31);
+    return __shfl_sync(kFull, x - x0, warp);
+  };
+  int n_hi, n_eq, n_lo;
+  const int hi_base = warp_prefix(0, n_hi);
+  const int eq_base = warp_prefix(16, n_eq);
+  const int lo_base = warp_prefix(32, n_lo);
+  // above -inf: entries >= X0 (all of them unless n_hi >= K); the -inf tier
+  // whole or its first m_eq columns; below -inf: entries >= X2
+  uint64_t X0 = 0, X2 = ~(uint64_t)0;
+  int m_eq = 0;
+  if (n_hi >= K || n_hi + n_eq < K) {
+    // the candidates of the tier that holds the K-th, in column order
+    const bool hi_tier = n_hi >= K;
+    int pos = hi_tier ? hi_base : lo_base;
+    for (int c = c_lo; c < c_hi; ++c) {
+      const int col = 32 * c + lane;
+      const uint32_t kq = key_at(col);
+      const bool in = hi_tier ? kq > kKeyNegInf : (col < L && kq < kKeyNegInf);
+      const uint32_t bal = __ballot_sync(kFull, in);
+      if (in) arr[pos + __popc(bal & lt)] = compose(kq, (uint32_t)(s + col));
+      pos += __popc(bal);
+    }
+    live_sync(nt);
+    if (hi_tier) {
+      X0 = smem_select(arr, n_hi, K, ss, hb, nt);
+    } else {
+      m_eq = n_eq;
+      X2 = smem_select(arr, n_lo, K - n_hi - n_eq, ss, hb, nt);
+    }
+  } else {
+    m_eq = K - n_hi;
+  }
+  // picked columns: count per warp, one prefix, then the writes
+  auto picked = [&](int col, uint32_t kq, int eq_rank) {
+    if (kq > kKeyNegInf) return compose(kq, (uint32_t)(s + col)) >= X0;
+    if (kq == kKeyNegInf) return eq_rank < m_eq;
+    return col < L && n_hi + n_eq < K && compose(kq, (uint32_t)(s + col)) >= X2;
+  };
+  int wsel = 0;
+  for (int c = c_lo, er = eq_base; c < c_hi; ++c) {
+    const int col = 32 * c + lane;
+    const uint32_t kq = key_at(col);
+    const uint32_t be = __ballot_sync(kFull, kq == kKeyNegInf);
+    wsel += __popc(__ballot_sync(kFull, picked(col, kq, er + __popc(be & lt))));
+    er += __popc(be);
+  }
+  // wt[48 ..) was never read, and the select's barriers ordered the reads above
+  if (lane == 0) wt[48 + warp] = wsel;
+  live_sync(nt);
+  int n_sel;
+  int o = warp_prefix(48, n_sel);
+  for (int c = c_lo, er = eq_base; c < c_hi; ++c) {
+    const int col = 32 * c + lane;
+    const uint32_t kq = key_at(col);
+    const uint32_t be = __ballot_sync(kFull, kq == kKeyNegInf);
+    const bool t = picked(col, kq, er + __popc(be & lt));
+    const uint32_t bs = __ballot_sync(kFull, t);
+    if (t && o + __popc(bs & lt) < K) out[o + __popc(bs & lt)] = (int32_t)(s + col);
+    o += __popc(bs);
+    er += __popc(be);
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------------
 // kernels
 
 // Dynamic shared memory of the select kernel:
@@ -776,16 +1174,8 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   uint64_t* keep = reinterpret_cast<uint64_t*>(dyn + (((size_t)p.bitmap_words * 4 + 15) & ~(size_t)15));
   uint8_t* region = reinterpret_cast<uint8_t*>(keep + p.Kb);
   uint64_t* buf = reinterpret_cast<uint64_t*>(region);
-
-  for (int i = threadIdx.x; i < p.bitmap_words; i += kThreads) bitmap[i] = 0;
-  if (threadIdx.x == 0) {
-    sh.cnt = 0;
-    sh.tau = 0;
-    sh.edge = 0;
-  }
   const Row R = load_row(p, r);
   float* rowp = p.logits + (int64_t)r * p.row_stride;
-  __syncthreads();
 
   // this CTA's share of the live blocks.  A row short enough for one CTA is
   // left to the leader alone: every CTA of the cluster computes the same
@@ -804,6 +1194,19 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
       j0 = j1 = 0;
     }
   }
+  // a short row on the 128-bit path stays in registers from end to end
+  if (parts == 1 && R.L <= kSmallCols && p.vec_log2g >= 0 && p.col_stride == 1 &&
+      (((uintptr_t)(rowp + R.s)) & 15u) == 0 &&
+      (int64_t)max(R.nb, min(R.L, p.cand_cap)) * 8 + (int64_t)R.L * 4 + 16 <= (int64_t)p.small_cap * 8) {
+    if (small_row<kTopK>(p, rowp, R, r, dyn)) return;
+  }
+  for (int i = threadIdx.x; i < p.bitmap_words; i += kThreads) bitmap[i] = 0;
+  if (threadIdx.x == 0) {
+    sh.cnt = 0;
+    sh.tau = 0;
+    sh.edge = 0;
+  }
+  __syncthreads();
   const bool clustered = kCluster && parts > 1;
   const int kk = clustered ? k : 1;
   stream_block_maxima(p, rowp, R, j0, j1, buf, keep, sh);
@@ -1376,13 +1779,15 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
       cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
     rc = DSA_ERR_CUDA;
   } else {
-    // CTAs per row: automatic = grow while the whole grid still fits in about
-    // one wave of two CTAs per SM and every CTA keeps >= kMinBlocksPerCta
-    // blocks of a full-width row; or the configured exact value.
+    // CTAs per row: automatic = grow while the grid still fits in one CTA
+    // per SM and every CTA keeps >= kMinBlocksPerCta blocks of a full-width
+    // row; or the configured exact value.  (A batch with a row per SM or more
+    // -- a decode batch -- runs one CTA per row: its rows are short, and the
+    // cluster launch would cost more than it saves.)
     int want = cfg->split;
     if (want == 0) {
       want = 1;
-      while (want < kMaxSplit && (int64_t)cfg->rows * want * 2 <= 2LL * sms &&
+      while (want < kMaxSplit && (int64_t)cfg->rows * want * 2 <= (int64_t)sms &&
              P.nblocks >= (int64_t)2 * want * kMinBlocksPerCta)
         want *= 2;
     }
@@ -1427,6 +1832,10 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
   pl->device = device;
   pl->sm_count = sms;
   pl->split = split;
+  // the short-row path keeps its scratch and candidates in the select
+  // kernel's dynamic shared memory
+  P.small_cap = P.vec_log2g >= 0 && z.select > sizeof(SmallScratch)
+                    ? (int32_t)((z.select - sizeof(SmallScratch)) / 8) : 0;
   pl->base = P;
   pl->smem_select = z.select;
   pl->smem_topk_cand = z.cand;
