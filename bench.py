@@ -318,10 +318,10 @@ def _events(torch, n):
     return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
 
 
-def measure_extras(dsa, torch, dev, local, prefill):
-    out = {}
+def measure_decode_graph(dsa, torch, dev, local, prefill):
+    """The 1M-width graph-captured decode: 96 rows, median end ~600; one CUDA
+    graph replay per step, warm and with L2 flushed."""
     peak, _ = hbm_peak()
-    # 1M-width graph-captured decode: 96 rows, median end ~600
     wl = wk.WORKLOADS["decode_1m"]
     x, starts, ends = wk.make_all(wl)
     logits = torch.from_numpy(x).to(dev)
@@ -361,34 +361,43 @@ def measure_extras(dsa, torch, dev, local, prefill):
     cold_us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(50))
     alg = int(algorithmic_bytes(wl, starts, ends, cand.cpu().numpy()).sum())
     full = wl.rows * wl.width * 4
-    out["decode_1m_graph"] = {
-        "rows": wl.rows, "us_per_replay_warm": warm_us, "us_per_replay_l2_flushed": cold_us,
-        "algorithmic_bytes": alg, "achieved_gbs_warm": alg / (warm_us * 1e-6) / 1e9,
-        "full_width_mask_bytes": full, "full_width_us_at_peak": full / (peak * 1e9) * 1e6}
-    del logits, flush, g
-    # one full 1M-column row (the pages' single-long-row case)
+    return {"rows": wl.rows, "us_per_replay_warm": warm_us, "us_per_replay_l2_flushed": cold_us,
+            "algorithmic_bytes": alg, "achieved_gbs_warm": alg / (warm_us * 1e-6) / 1e9,
+            "full_width_mask_bytes": full, "full_width_us_at_peak": full / (peak * 1e9) * 1e6,
+            "ctas": plan.describe()["grid_select"]}
+
+
+def measure_single_row(dsa, torch, dev, local, prefill):
+    """One full 1M-column row (the pages' single-long-row case), fresh input
+    every call."""
     wl1 = wk.WORKLOADS["prefill_1m"].with_(rows=1)
     x1 = wk.make_rows(wl1, [0], None, np.array([wl1.width], dtype=np.int32))
     l1 = torch.from_numpy(x1).to(dev)
+    pristine = l1.clone()
     e1d = torch.tensor([wl1.width], dtype=torch.int32, device=dev)
     c1 = torch.empty((1, wl1.block_topk + 1), dtype=torch.int32, device=dev)
     t1 = torch.empty((1, wl1.row_topk), dtype=torch.int32, device=dev)
     p1 = dsa.dsa_select_init(device=local, rows=1, width=wl1.width, block_size=wl1.block_size,
                              block_topk=wl1.block_topk, row_topk=wl1.row_topk)
     for _ in range(3):
+        l1.copy_(pristine)
         dsa.dsa_select_topk(p1, l1, None, e1d, c1, t1)
-    e0, e1 = _events(torch, 2)
-    e0.record()
-    for _ in range(20):
+    ev = _events(torch, 40)
+    for i in range(20):
+        l1.copy_(pristine)
+        ev[2 * i].record()
         dsa.dsa_select_topk(p1, l1, None, e1d, c1, t1)
-    e1.record()
+        ev[2 * i + 1].record()
     torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / 20
+    us = statistics.median(ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3 for i in range(20))
     a1 = int(algorithmic_bytes(wl1, None, np.array([wl1.width], dtype=np.int32),
                                c1.cpu().numpy()).sum())
-    out["single_row_1m"] = {"us_per_call": us, "achieved_gbs": a1 / (us * 1e-6) / 1e9,
-                            "ctas": p1.describe()["grid_select"]}
-    # scan-mode row top-k over the (masked) prefill logits
+    return {"us_per_call": us, "achieved_gbs": a1 / (us * 1e-6) / 1e9,
+            "ctas": p1.describe()["grid_select"], "input": "fresh row every call"}
+
+
+def measure_scan(dsa, torch, dev, local, prefill):
+    """Scan-mode row top-k over the (masked) prefill logits."""
     wlp, plan_p, logits_p, ends_p, topk_p = prefill
     out_t = torch.empty_like(topk_p)
     dsa.dsa_row_topk(plan_p, logits_p, None, ends_p, None, out_t)
@@ -402,11 +411,16 @@ def measure_extras(dsa, torch, dev, local, prefill):
     _, e = row_bounds(wlp, None, ends_p.cpu().numpy())
     L = np.minimum(e, wlp.width)
     scan_alg = int((4 * L + 4 * wlp.row_topk + 8).sum())
-    out["scan_topk_prefill_1m"] = {
-        "ms_per_launch": ms, "rows_per_s": wlp.rows / (ms / 1e3),
-        "achieved_gbs": scan_alg / (ms / 1e3) / 1e9,
-        "matches_fused": bool(torch.equal(out_t, topk_p))}
-    # top-k / sliding-window combine on the prefill chunk's top-k
+    peak, _ = hbm_peak()
+    return {"ms_per_launch": ms, "rows_per_s": wlp.rows / (ms / 1e3),
+            "achieved_gbs": scan_alg / (ms / 1e3) / 1e9,
+            "frac": scan_alg / (ms / 1e3) / 1e9 / peak,
+            "matches_fused": bool(torch.equal(out_t, topk_p))}
+
+
+def measure_combine(dsa, torch, dev, local, prefill):
+    """Top-k / sliding-window combine on the prefill chunk's top-k."""
+    wlp, plan_p, logits_p, ends_p, topk_p = prefill
     window = 128
     comb = torch.empty((wlp.rows, wlp.row_topk + window), dtype=torch.int32, device=dev)
     for _ in range(3):
@@ -419,13 +433,29 @@ def measure_extras(dsa, torch, dev, local, prefill):
     torch.cuda.synchronize()
     us = e0.elapsed_time(e1) * 1e3 / 20
     comb_alg = wlp.rows * (4 * wlp.row_topk + 4 * (wlp.row_topk + window) + 8)
-    out["combine_window_prefill_1m"] = {"window": window, "us_per_launch": us,
-                                        "achieved_gbs": comb_alg / (us * 1e-6) / 1e9}
-    out["indexer_producer"] = measure_producer(dsa, torch, dev)
-    out["indexer_select_fused"] = measure_fused(dsa, torch, dev)
-    out["indexer_select_fused_96x1m"] = measure_fused(dsa, torch, dev, T=96, S=1 << 20)
-    out["grouped_sparse_attention"] = measure_attention(dsa, torch, dev)
-    return out
+    peak, _ = hbm_peak()
+    return {"window": window, "us_per_launch": us, "achieved_gbs": comb_alg / (us * 1e-6) / 1e9,
+            "frac": comb_alg / (us * 1e-6) / 1e9 / peak}
+
+
+# supplementary measurements (not the bench metric), by name
+EXTRAS = {
+    "decode_1m_graph": measure_decode_graph,
+    "single_row_1m": measure_single_row,
+    "scan_topk_prefill_1m": measure_scan,
+    "combine_window_prefill_1m": measure_combine,
+    "indexer_producer": lambda dsa, torch, dev, local, prefill: measure_producer(dsa, torch, dev),
+    "indexer_select_fused": lambda dsa, torch, dev, local, prefill: measure_fused(dsa, torch, dev),
+    "indexer_select_fused_96x1m": lambda dsa, torch, dev, local, prefill: measure_fused(
+        dsa, torch, dev, T=96, S=1 << 20),
+    "grouped_sparse_attention": lambda dsa, torch, dev, local, prefill: measure_attention(
+        dsa, torch, dev),
+}
+
+
+def measure_extras(dsa, torch, dev, local, prefill, names=None):
+    return {name: fn(dsa, torch, dev, local, prefill) for name, fn in EXTRAS.items()
+            if names is None or name in names}
 
 
 def fp8_peak_tflops():
@@ -716,7 +746,7 @@ def run_ours(args, wl):
     }
     if args.extras:
         line["extras"] = measure_extras(dsa, torch, dev, local,
-                                        (wl, plan, logits, ends_d, topk))
+                                        (wl, plan, logits, ends_d, topk), args.extra)
     if args.cpu_rows > 0:
         cores = host_cores()
         rng = np.random.default_rng(1)
@@ -752,6 +782,8 @@ def main():
                     help="time only the grouped masked sparse attention and print its JSON")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the supplementary decode / single-row / scan-mode timings")
+    ap.add_argument("--extra", action="append", choices=sorted(EXTRAS),
+                    help="run only the named supplementary timing (repeatable)")
     ap.add_argument("--rows", type=int, default=None,
                     help="override the workload's row count (smaller profiling cases)")
     ap.add_argument("--cpu-rows", type=int, default=384,
