@@ -44,6 +44,7 @@ constexpr uint32_t kNegInfBits = 0xFF800000u;
 constexpr uint32_t kKeyNegInf = 0x007FFFFFu;  // order_key(-inf)
 constexpr uint32_t kFillerBits = 0xFFFFFFFFu; // order_key == 0: below every value
 constexpr int kVecPerThread = 4;              // float4 loads in flight per thread per round
+constexpr int kPrefetchRounds = 2;            // L2 bulk prefetch distance of the streaming loop, in rounds
 constexpr int kBlocksPerThreadGeneric = 2;    // blocks per thread per round, scalar path
 constexpr int kMaxTopK = 4096;
 constexpr int kMaxBlockTopK = 4096;
@@ -407,6 +408,17 @@ __device__ void stream_block_maxima(const Params& p, const float* rowp, const Ro
     };
     float4 x[kVecPerThread];
     int32_t rb = j0 << g_log2;
+    // one thread keeps L2 kPrefetchRounds rounds ahead of the loads (a bulk
+    // prefetch of one round, kThreads * kVecPerThread vectors, per round), so
+    // the loads find their lines in L2 and HBM sees more bytes in flight
+    auto prefetch = [&](int32_t pv) {
+      if (threadIdx.x == 0 && pv < v_full) {
+        const int32_t pn = min(VR, v_full - pv);
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(vp + pv), "r"(pn * 16) : "memory");
+      }
+    };
+#pragma unroll 1
+    for (int d = 1; d <= kPrefetchRounds; ++d) prefetch(rb + d * VR);
     if (rb < v_end) load_round(rb, x);
     // epochs of p.epoch rounds: the buffer absorbs a whole epoch's worst-case
     // insertions, so the CTA synchronises (and maybe compacts) once per epoch
@@ -421,6 +433,7 @@ __device__ void stream_block_maxima(const Params& p, const float* rowp, const Ro
       for (int e = 0; e < ep && rb < v_end; ++e) {
         const int32_t nrb = rb + VR;
         float4 y[kVecPerThread];
+        prefetch(rb + (kPrefetchRounds + 1) * VR);
         if (nrb < v_end) load_round(nrb, y);
 #pragma unroll
         for (int u = 0; u < kVecPerThread; ++u) {
