@@ -709,29 +709,58 @@ def run_ours(args, wl):
     del pristine, flush
 
     # end to end through the public API: pinned host logits -> device, the
-    # fused call, cand + topk -> pinned host, every step
+    # fused call, cand + topk -> pinned host, every step.  The rows go in
+    # chunks: the copy of chunk c + 1 (a second stream) overlaps the call on
+    # chunk c, and each chunk's outputs go back as soon as its call is done.
     e2e = None
     if args.e2e_steps > 0:
+        cand_ref, topk_ref = cand.clone(), topk.clone()
         cand_out = torch.empty(cand.shape, dtype=torch.int32, pin_memory=True)
         topk_out = torch.empty(topk.shape, dtype=torch.int32, pin_memory=True)
+        rep = wl.row_repeat
+        chunks = max(1, min(args.e2e_chunks, wl.rows // rep))
+        per = -(-(wl.rows // rep) // chunks) * rep
+        pieces = []
+        for r0 in range(0, wl.rows, per):
+            r1 = min(r0 + per, wl.rows)
+            pl = dsa.dsa_select_init(device=local, rows=r1 - r0, width=wl.width,
+                                     block_size=wl.block_size, block_topk=wl.block_topk,
+                                     row_topk=wl.row_topk, row_repeat=rep)
+            pieces.append((r0, r1, pl, torch.cuda.Event()))
+        copier = torch.cuda.Stream()
+
+        def e2e_step():
+            copier.wait_stream(stream)  # the previous step's calls are done with the rows
+            for r0, r1, pl, ev in pieces:
+                with torch.cuda.stream(copier):
+                    logits[r0:r1].copy_(host[r0:r1], non_blocking=True)
+                    ends_d[r0 // rep:-(-r1 // rep)].copy_(ends_h[r0 // rep:-(-r1 // rep)],
+                                                          non_blocking=True)
+                    ev.record(copier)
+                stream.wait_event(ev)
+                dsa.dsa_select_topk(pl, logits[r0:r1], None, ends_d[r0 // rep:-(-r1 // rep)],
+                                    cand[r0:r1], topk[r0:r1], stream=stream)
+                cand_out[r0:r1].copy_(cand[r0:r1], non_blocking=True)
+                topk_out[r0:r1].copy_(topk[r0:r1], non_blocking=True)
+
+        e2e_step()  # warm-up (plans, copies)
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier()
         torch.cuda.synchronize()
         e0.record(stream)
         for _ in range(args.e2e_steps):
-            logits.copy_(host, non_blocking=True)
-            ends_d.copy_(ends_h, non_blocking=True)
-            step()
-            cand_out.copy_(cand, non_blocking=True)
-            topk_out.copy_(topk, non_blocking=True)
+            e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
         h2d = host.numel() * 4 + ends_h.numel() * 4
         d2h = cand_out.numel() * 4 + topk_out.numel() * 4
+        same = bool(torch.equal(cand_out, cand_ref.cpu()) and torch.equal(topk_out, topk_ref.cpu()))
         e2e = {"value": wl.rows * world * args.e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps}
+               "ms_per_step": e2e_ms / args.e2e_steps, "steps": args.e2e_steps,
+               "chunks": len(pieces), "matches_single_call": same}
 
     if rank != 0:
         return
@@ -792,6 +821,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="prefill_1m", choices=sorted(wk.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="row chunks of the end-to-end step (copy of one overlaps the call on another)")
     ap.add_argument("--producer-only", nargs=2, type=int, metavar=("QUERIES", "KEYS"),
                     help="time only the tensor-core indexer-logits producer and print its JSON")
     ap.add_argument("--fused-only", nargs=2, type=int, metavar=("QUERIES", "KEYS"),
