@@ -1070,14 +1070,17 @@ __device__ __noinline__ bool small_row(const Params& p, float* rowp, const Row& 
   const int c_lo = min(warp * cpw, nck), c_hi = min(c_lo + cpw, nck);
   const uint32_t lt = lanemask_lt();
   auto key_at = [&](int col) { return col < L ? keys[col] : 0u; };
-  int whi = 0, weq = 0, wlo = 0;
+  uint32_t mhi = 0, meq = 0, mlo = 0;  // this lane's counts, summed over the warp below
   for (int c = c_lo; c < c_hi; ++c) {
     const int col = 32 * c + lane;
     const uint32_t kq = key_at(col);
-    whi += __popc(__ballot_sync(kFull, kq > kKeyNegInf));
-    weq += __popc(__ballot_sync(kFull, kq == kKeyNegInf));
-    wlo += __popc(__ballot_sync(kFull, col < L && kq < kKeyNegInf));
+    mhi += kq > kKeyNegInf;
+    meq += kq == kKeyNegInf;
+    mlo += col < L && kq < kKeyNegInf;
   }
+  const int whi = (int)__reduce_add_sync(kFull, mhi);
+  const int weq = (int)__reduce_add_sync(kFull, meq);
+  const int wlo = (int)__reduce_add_sync(kFull, mlo);
   int32_t* wt = ss.chunk[0];  // [0, 16): above -inf, [16, 32): -inf, [32, 48): below, [48, 64): picked
   if (lane == 0) {
     wt[warp] = whi;
@@ -1133,14 +1136,15 @@ __device__ __noinline__ bool small_row(const Params& p, float* rowp, const Row& 
     if (kq == kKeyNegInf) return eq_rank < m_eq;
     return col < L && n_hi + n_eq < K && compose(kq, (uint32_t)(s + col)) >= X2;
   };
-  int wsel = 0;
+  uint32_t msel = 0;
   for (int c = c_lo, er = eq_base; c < c_hi; ++c) {
     const int col = 32 * c + lane;
     const uint32_t kq = key_at(col);
     const uint32_t be = __ballot_sync(kFull, kq == kKeyNegInf);
-    wsel += __popc(__ballot_sync(kFull, picked(col, kq, er + __popc(be & lt))));
+    msel += picked(col, kq, er + __popc(be & lt));
     er += __popc(be);
   }
+  const int wsel = (int)__reduce_add_sync(kFull, msel);
   // wt[48 ..) was never read, and the select's barriers ordered the reads above
   if (lane == 0) wt[48 + warp] = wsel;
   live_sync(nt);
