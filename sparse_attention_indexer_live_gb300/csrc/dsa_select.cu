@@ -1130,6 +1130,34 @@ __device__ __noinline__ bool small_row(const Params& p, float* rowp, const Row& 
   } else {
     m_eq = K - n_hi;
   }
+  if (n_hi >= K) {
+    // the K picks are the entries of arr (the values above -inf, in column
+    // order) at or above X0: each warp takes a run of arr's 32-entry chunks,
+    // counts what it drops, and writes the rest shifted down past the drops
+    const int nck2 = (n_hi + 31) >> 5;
+    const int cpw2 = (nck2 + kWarps - 1) / kWarps;
+    const int a_lo = min(warp * cpw2, nck2), a_hi = min(a_lo + cpw2, nck2);
+    uint32_t mdrop = 0;
+    for (int c = a_lo; c < a_hi; ++c) {
+      const int i = 32 * c + lane;
+      mdrop += i < n_hi && arr[i] < X0;
+    }
+    const int wdrop = (int)__reduce_add_sync(kFull, mdrop);
+    if (lane == 0) wt[48 + warp] = wdrop;
+    live_sync(nt);
+    int n_drop;
+    int dropped = warp_prefix(48, n_drop);  // drops before this warp's run
+    for (int c = a_lo; c < a_hi; ++c) {
+      const int i = 32 * c + lane;
+      const uint64_t a = i < n_hi ? arr[i] : 0;
+      const bool drop = i < n_hi && a < X0;
+      const uint32_t bd = __ballot_sync(kFull, drop);
+      const int o = i - dropped - __popc(bd & lt);
+      if (i < n_hi && !drop && o < K) out[o] = (int32_t)comp_index(a);
+      dropped += __popc(bd);
+    }
+    return true;
+  }
   // picked columns: count per warp, one prefix, then the writes
   auto picked = [&](int col, uint32_t kq, int eq_rank) {
     if (kq > kKeyNegInf) return compose(kq, (uint32_t)(s + col)) >= X0;
