@@ -815,12 +815,15 @@ __device__ uint64_t smem_select(const uint64_t* a, int n, int k, SmallScratch& s
     }
     live_sync(nt);
     uint32_t hv[8];
+    {
+      const uint4 h0 = reinterpret_cast<const uint4*>(h)[2 * lane];
+      const uint4 h1 = reinterpret_cast<const uint4*>(h)[2 * lane + 1];
+      hv[0] = h0.x; hv[1] = h0.y; hv[2] = h0.z; hv[3] = h0.w;
+      hv[4] = h1.x; hv[5] = h1.y; hv[6] = h1.z; hv[7] = h1.w;
+    }
     uint32_t tot = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      hv[q] = h[8 * lane + q];
-      tot += hv[q];
-    }
+    for (int q = 0; q < 8; ++q) tot += hv[q];
     uint32_t incl = tot;  // entries in this lane's bins and every higher lane's
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -828,15 +831,15 @@ __device__ uint64_t smem_select(const uint64_t* a, int n, int k, SmallScratch& s
       if (lane + o < 32) incl += y;
     }
     uint32_t cum = incl - tot;
+    // the crossing bin is unique: branch-free selects, no carried flag
     uint32_t found = 0, d = 0, above = 0, cntd = 0;
 #pragma unroll
     for (int q = 7; q >= 0; --q) {
-      if (!found && cum < kk && cum + hv[q] >= kk) {
-        found = 1;
-        d = (uint32_t)(8 * lane + q);
-        above = cum;
-        cntd = hv[q];
-      }
+      const bool hit = cum < kk && cum + hv[q] >= kk;
+      d = hit ? (uint32_t)(8 * lane + q) : d;
+      above = hit ? cum : above;
+      cntd = hit ? hv[q] : cntd;
+      found |= hit;
       cum += hv[q];
     }
     const int src = __ffs(__ballot_sync(kFull, found)) - 1;
