@@ -808,7 +808,11 @@ __device__ uint64_t smem_select(const uint64_t* a, int n, int k, SmallScratch& s
   for (int shift = 56; shift >= 0; shift -= 8) {
     uint32_t* h = ss.hist[b];
     const int nbuf = b == 2 ? 0 : b + 1;
-    for (int i = threadIdx.x; i < 256; i += nt) ss.hist[nbuf][i] = 0u;
+    if (nt >= 256) {
+      if (threadIdx.x < 256) ss.hist[nbuf][threadIdx.x] = 0u;
+    } else {
+      for (int i = threadIdx.x; i < 256; i += nt) ss.hist[nbuf][i] = 0u;
+    }
     for (int i = threadIdx.x; i < n; i += nt) {
       const uint64_t c = a[i];
       if ((c & mask) == prefix) atomicAdd(&h[(uint32_t)(c >> shift) & 0xFFu], 1u);
@@ -1084,10 +1088,11 @@ __device__ __noinline__ bool small_row(const Params& p, float* rowp, const Row& 
   const int whi = (int)__reduce_add_sync(kFull, mhi);
   const int weq = (int)__reduce_add_sync(kFull, meq);
   const int wlo = (int)__reduce_add_sync(kFull, mlo);
-  int32_t* wt = ss.chunk[0];  // [0, 16): above -inf, [16, 32): -inf, [32, 48): below, [48, 64): picked
+  // [0, 16): above -inf in the low half, -inf in the high half (each count is
+  // at most 8192, so one scan sums both); [32, 48): below; [48, 64): picked
+  int32_t* wt = ss.chunk[0];
   if (lane == 0) {
-    wt[warp] = whi;
-    wt[16 + warp] = weq;
+    wt[warp] = whi | (weq << 16);
     wt[32 + warp] = wlo;
   }
   live_sync(nt);
@@ -1103,10 +1108,11 @@ __device__ __noinline__ bool small_row(const Params& p, float* rowp, const Row& 
     total = __shfl_sync(kFull, x, 31);
     return __shfl_sync(kFull, x - x0, warp);
   };
-  int n_hi, n_eq, n_lo;
-  const int hi_base = warp_prefix(0, n_hi);
-  const int eq_base = warp_prefix(16, n_eq);
+  int n_he, n_lo;
+  const int he_base = warp_prefix(0, n_he);
   const int lo_base = warp_prefix(32, n_lo);
+  const int n_hi = n_he & 0xFFFF, n_eq = n_he >> 16;
+  const int hi_base = he_base & 0xFFFF, eq_base = he_base >> 16;
   // above -inf: entries >= X0 (all of them unless n_hi >= K); the -inf tier
   // whole or its first m_eq columns; below -inf: entries >= X2
   uint64_t X0 = 0, X2 = ~(uint64_t)0;
