@@ -572,12 +572,23 @@ def measure_attention(dsa, torch, dev, T=2048, H=8, S=1 << 20, Kc=2048, own=0.05
     scale = 1.0 / math.sqrt(128)
 
     def timed(f, reps=20):
-        for _ in range(3):
-            f()
+        # reps calls captured in one CUDA graph: the replay times the kernels,
+        # not the host's launch rate
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                f()
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(reps):
+                f()
+        g.replay()
+        torch.cuda.synchronize()
         e0, e1 = _events(torch, 2)
         e0.record()
-        for _ in range(reps):
-            f()
+        g.replay()
         e1.record()
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / reps

@@ -253,7 +253,7 @@ int dsa_indexer_select(const dsa_select_plan* plan, const dsa_indexer_cfg* cfg, 
  *   heads      8 or 16 (G = 16 or 8);  head_dim = value_dim = 128
  *   keys       S: rows of k and v
  *   select     Kc: entries per token in idx, with G * Kc <= 49,152 (a group's
- *              rows are merged in shared memory)
+ *              union's token masks are built in shared memory)
  *   idx        int32 [tokens, Kc]: each row's positions in [0, S), strictly
  *              ascending, then -1 for unused entries (the rows dsa_row_topk
  *              and dsa_combine_window write qualify)

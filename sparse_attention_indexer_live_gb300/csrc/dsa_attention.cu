@@ -9,11 +9,9 @@
 // tokens that selected each) and the attention over it.
 //
 // Design (this file's own):
-//   * union: one CTA per group stages the group's rows in shared memory, cuts
-//     key space into 512 ranges (one per thread) and merges each range's
-//     pieces of the rows once, with the rows' heads in registers; output goes
-//     to provisional slots and is compacted after a block-wide prefix (no
-//     atomics);
+//   * union: one CTA per group sets a bit per selected key in a bitmap of key
+//     space in shared memory, scans it for the union's ranks (written out
+//     ascending), then ORs each entry's token bit into the mask of its rank;
 //   * attention: one CTA per group of 128 query/head rows, walking the union
 //     in tiles of 128 positions.  Loader warps gather the tile's key and
 //     value rows (cp.async, whole 256-byte rows per half-warp, two tiles in
@@ -40,10 +38,9 @@
 namespace {
 
 constexpr int kRows = 128;                 // tokens x heads per group = one MMA tile of rows
-constexpr int kUThreads = 512;
+constexpr int kUThreads = 1024;
 constexpr int kUWarps = kUThreads / 32;
-constexpr int kMaxUG = 16;                 // tokens per group (G = 128 / H, H >= 8)
-constexpr int64_t kMaxUnionRows = 49152;   // G * Kc positions staged in shared memory (192 KB + 16 KB starts)
+constexpr int64_t kMaxUnionRows = 49152;   // G * Kc: the masks of a group's union in shared memory (96 KB)
 
 __host__ __device__ constexpr int64_t align16(int64_t x) { return (x + 15) & ~(int64_t)15; }
 
@@ -92,177 +89,233 @@ __device__ int block_scan(int v, int* total, int* wtot) {
   return base + x - v;
 }
 
-__device__ __forceinline__ uint32_t su32_u(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+// Union of one group's selections through a bitmap of key space in shared
+// memory: a bit per key (32-bit words), a 16-bit rank prefix per word and a
+// summary bit per 128-key group that is not empty.  Key space is taken in
+// chunks (all of [0, S) at once when it fits):
+//   1. every valid entry of the group's rows in the chunk sets its key's bit
+//      (shared atomic OR);
+//   2. one linear pass marks the groups that are not empty in the summary;
+//      the scan then visits those groups only: their set bits, an exclusive
+//      prefix over the block, each word's prefix (16 bits: a chunk's union is
+//      at most G * Kc <= 49,152) and the chunk's keys written to the record,
+//      ascending;
+//   3. a pass over the entries takes each one's rank from its word's prefix
+//      and the bits below it and ORs its token's bit into the mask of that
+//      rank.  The masks live in the shared memory after the bitmap, 32 bits a
+//      rank when the chunk's union fits there, else 16 bits (G <= 16), two to
+//      a word, one window of ranks per pass.
+// Set semantics throughout: rows in any order, repeated entries and entries
+// outside [0, S) (dropped) give the union the definition gives, and nothing
+// can write past the record (the union is at most the valid entries).  When
+// [0, S) takes more than two chunks, a first pass finds the smallest and
+// largest valid entry so that only the chunks between them are scanned.
+// Dynamic shared memory: bits [chunk / 32] uint32 | pre [chunk / 32] uint16 |
+// summary [chunk / 4096] uint32 | masks.
+constexpr int kUChunkQuant = 32768;                // keys per chunk: a multiple of this
+constexpr int kUSmemBudget = 227 * 1024 - 1024;    // dynamic shared memory a union launch may take (+ static)
+constexpr int kUMinMaskBytes = 16 * 1024;          // the smallest mask area (8,192 ranks of 16 bits)
+constexpr int kUBatch = 8;                         // 16-byte entry loads in flight per thread
 
-// Union of one group's selections by a multi-way merge.  The group's rows
-// (ascending positions, then -1 padding) are staged in shared memory.  Key
-// space is cut into 512 ranges by a shift of the key; thread s owns range s.
-// One coalesced pass over every row records, per row and range, where the
-// row enters the range (a row's entries of range s are [start[s],
-// start[s + 1])).  Each thread then merges its pieces once, holding the
-// current head of every row in a register so that only the rows it advances
-// are read again: every distinct position once, with the bits of the tokens
-// whose rows hold it.  The merged output goes to provisional slots (a prefix
-// of the pieces' sizes, which bound it); a block-wide prefix of the real
-// counts then gives the final ranks and the output is compacted through the
-// shared memory the rows occupied -- no atomics.
-// Dynamic shared memory: rows [G][Kc] int32 | start [G][513] uint16.
-constexpr int kUBuckets = kUThreads;
+struct UnionShape {
+  int32_t chunk;    // keys per chunk
+  int32_t pre_off;  // byte offsets in dynamic shared memory
+  int32_t sum_off;
+  int32_t m_off;
+  int32_t m_bytes;  // the mask area
+  int32_t smem;
+};
 
-__device__ __forceinline__ int ubucket(int32_t key, int shift) {
-  return min(max(key, 0) >> shift, kUBuckets - 1);
+inline UnionShape union_shape(int G, int Kc, int S) {
+  const int64_t cap = (int64_t)G * Kc;
+  // 97/512 byte per key: its bit, a 16-bit prefix per 32 keys, a summary bit
+  // per 128 keys
+  int64_t most = (int64_t)(kUSmemBudget - kUMinMaskBytes) * 512 / 97;
+  most -= most % kUChunkQuant;
+  const int64_t need = ((int64_t)std::max(S, 1) + kUChunkQuant - 1) / kUChunkQuant * kUChunkQuant;
+  UnionShape u;
+  u.chunk = (int32_t)std::min(most, need);
+  u.pre_off = u.chunk / 8;
+  u.sum_off = u.pre_off + u.chunk / 16;
+  u.m_off = u.sum_off + u.chunk / 1024;
+  // 32-bit masks for every rank when they fit, else what is left
+  u.m_bytes = (int32_t)std::min<int64_t>(align16(cap * 4), kUSmemBudget - u.m_off);
+  u.smem = u.m_off + u.m_bytes;
+  return u;
 }
 
-// head = lists[addr] when p, else unchanged (no branch)
-__device__ __forceinline__ int32_t lds_if(bool p, uint32_t addr, int32_t head) {
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.u32 q, %2, 0;\n @q ld.shared.b32 %0, [%1];\n}\n"
-      : "+r"(head)
-      : "r"(addr), "r"((uint32_t)p)
-      : "memory");
-  return head;
-}
-
-template <int kG>
 __global__ void __launch_bounds__(kUThreads)
-    union_kernel(const int32_t* idx, int32_t T, int32_t Kc, int32_t S, uint8_t* ws, UnionLayout L) {
-  extern __shared__ __align__(16) int32_t lists[];
+    union_kernel(const int32_t* idx, int32_t T, int32_t Kc, int32_t S, int32_t G, uint8_t* ws, UnionLayout L,
+                 UnionShape U) {
+  extern __shared__ __align__(16) uint8_t usm[];
   __shared__ int wtot[kUWarps + 1];
-  __shared__ int len[kG];
+  __shared__ int s_lo, s_hi;
+  uint32_t* bits = reinterpret_cast<uint32_t*>(usm);
+  uint16_t* pre = reinterpret_cast<uint16_t*>(usm + U.pre_off);
+  uint32_t* summary = reinterpret_cast<uint32_t*>(usm + U.sum_off);
+  uint32_t* m32 = reinterpret_cast<uint32_t*>(usm + U.m_off);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = blockIdx.x;
-  const int t0 = grp * kG;
-  const int nt = min(kG, T - t0);
+  const int t0 = grp * G;
+  const int nt = min(G, T - t0);
   uint8_t* rec = ws + (int64_t)grp * L.bytes;
   int32_t* keys = reinterpret_cast<int32_t*>(rec + L.keys_off);
   uint32_t* masks = reinterpret_cast<uint32_t*>(rec + L.masks_off);
   const int32_t* rows = idx + (int64_t)t0 * Kc;
-  const int cap = kG * Kc;
-  uint16_t* start = reinterpret_cast<uint16_t*>(lists + cap);
-  // key >> shift < 512 for every key in [0, S)
-  int shift = 0;
-  while (((int64_t)(S - 1) >> shift) >= kUBuckets) ++shift;
-
-  // stage the rows: one contiguous block of nt Kc entries (every copy of a
-  // thread in flight at once)
-  const int total_in = nt * Kc;
-  if ((Kc & 3) == 0 && (reinterpret_cast<uintptr_t>(rows) & 15) == 0) {
-    for (int i = 4 * threadIdx.x; i < total_in; i += 4 * kUThreads)
-      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32_u(lists + i)), "l"(rows + i) : "memory");
-  } else {
-    for (int i = threadIdx.x; i < total_in; i += kUThreads)
-      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(su32_u(lists + i)), "l"(rows + i) : "memory");
-  }
-  asm volatile("cp.async.commit_group;\n cp.async.wait_group 0;" ::: "memory");
-  __syncthreads();
-  // a row's length: its entries are valid (>= 0) up to the padding
-  if (threadIdx.x < nt) {
-    const int32_t* row = lists + threadIdx.x * Kc;
-    int lo = 0, hi = Kc;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (row[mid] >= 0) lo = mid + 1; else hi = mid;
-    }
-    len[threadIdx.x] = lo;
-  }
-  __syncthreads();
-  // where each row enters each range: entry i writes the ranges between its
-  // predecessor's and its own, so that start[s] = first entry of range >= s.
-  // Neighbouring entries mostly share a range or sit in adjacent ones: one
-  // write, and a loop only across empty ranges.
-#pragma unroll 1
-  for (int g = 0; g < nt; ++g) {
-    const int n = len[g];
-    const int32_t* row = lists + g * Kc;
-    uint16_t* st = start + g * (kUBuckets + 1);
-    for (int i0 = 4 * threadIdx.x; i0 <= n; i0 += 4 * kUThreads) {
-      int b[5];
-      b[0] = i0 == 0 ? -1 : ubucket(row[i0 - 1], shift);
+  const int total_in = nt * Kc;  // <= 49,152: exact in fp32
+  const float inv_kc = 1.0f / (float)max(Kc, 1);
+  const bool vec = (Kc & 3) == 0 && (reinterpret_cast<uintptr_t>(rows) & 15) == 0;
+  // i / Kc (i < 2^24) from the fp32 quotient, off by at most one, corrected
+  auto row_of = [&](int i) {
+    int t = __float2int_rz((float)i * inv_kc);
+    t -= t * Kc > i;
+    t += (t + 1) * Kc <= i;
+    return t;
+  };
+  // f(entry, token) for every entry of the group's rows, kUBatch 16-byte
+  // loads of a thread in flight at once (four entries of one row each)
+  auto for_entries = [&](auto&& f) {
+    if (vec) {
+      for (int i0 = 4 * tid; i0 < total_in; i0 += 4 * kUThreads * kUBatch) {
+        int4 v[kUBatch];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) b[u + 1] = i0 + u < n ? ubucket(row[i0 + u], shift) : kUBuckets;
+        for (int u = 0; u < kUBatch; ++u) {
+          const int i = i0 + 4 * kUThreads * u;
+          v[u] = i < total_in ? __ldg(reinterpret_cast<const int4*>(rows + i)) : make_int4(-1, -1, -1, -1);
+        }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int i = i0 + u;
-        if (i <= n && b[u + 1] > b[u]) {
-          st[b[u] + 1] = (uint16_t)i;
-          for (int x = b[u] + 2; x <= b[u + 1]; ++x) st[x] = (uint16_t)i;
+        for (int u = 0; u < kUBatch; ++u) {
+          const int t = row_of(i0 + 4 * kUThreads * u);
+          f(v[u].x, t);
+          f(v[u].y, t);
+          f(v[u].z, t);
+          f(v[u].w, t);
         }
       }
+    } else {
+      for (int i = tid; i < total_in; i += kUThreads) f(__ldg(rows + i), row_of(i));
     }
-  }
-  __syncthreads();
-  // this thread's piece of each row; the clamps keep rows that break the
-  // contract (unsorted) inside the row
-  int q[kG], end[kG];
-  int pieces = 0;
-#pragma unroll
-  for (int g = 0; g < kG; ++g) {
-    q[g] = end[g] = 0;
-    if (g < nt) {
-      const uint16_t* st = start + g * (kUBuckets + 1);
-      q[g] = min((int)st[threadIdx.x], len[g]);
-      end[g] = max(q[g], min((int)st[threadIdx.x + 1], len[g]));
-      pieces += end[g] - q[g];
-    }
-  }
-  int total = 0;
-  const int prov = block_scan(pieces, &total, wtot);
-  // merge into the provisional slots [prov, prov + pieces)
-  int32_t head[kG];
-  uint32_t addr[kG];
-#pragma unroll
-  for (int g = 0; g < kG; ++g) {
-    addr[g] = su32_u(lists + g * Kc + q[g]);
-    head[g] = lds_if(q[g] < end[g], addr[g], INT32_MAX);
-  }
-  int out = 0;
-  while (true) {
-    int32_t mn[kG];
-#pragma unroll
-    for (int g = 0; g < kG; ++g) mn[g] = head[g];
-#pragma unroll
-    for (int w = kG / 2; w >= 1; w >>= 1)
-#pragma unroll
-      for (int g = 0; g < w; ++g) mn[g] = min(mn[g], mn[g + w]);
-    const int32_t key = mn[0];
-    if (key == INT32_MAX) break;
-    uint32_t m = 0;
-#pragma unroll
-    for (int g = 0; g < kG; ++g) {
-      const bool hit = head[g] == key;
-      m |= (uint32_t)hit << g;
-      q[g] += hit;
-      addr[g] += hit ? 4u : 0u;
-      const bool more = q[g] < end[g];
-      head[g] = lds_if(hit && more, addr[g], hit && !more ? INT32_MAX : head[g]);
-    }
-    if (key >= 0 && key < S && prov + out < cap) {
-      keys[prov + out] = key;
-      masks[prov + out] = m;
-      ++out;
-    }
-  }
-  // final ranks; rows that break the contract cannot push the union past the
-  // record or make it name a key outside [0, S)
-  int n = 0;
-  const int fin = block_scan(out, &n, wtot);
-  if (threadIdx.x == 0) *reinterpret_cast<int32_t*>(rec) = n;
-  // compact keys, then masks, through the rows' shared memory (the reads of
-  // a thread's provisional slots go out eight at a time)
-  for (int half = 0; half < 2; ++half) {
-    uint32_t* src = half == 0 ? reinterpret_cast<uint32_t*>(keys) : masks;
-    uint32_t* stage = reinterpret_cast<uint32_t*>(lists);
-    __syncthreads();
-    for (int j0 = 0; j0 < out; j0 += 8) {
-      uint32_t x[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) x[u] = j0 + u < out ? src[prov + j0 + u] : 0u;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (j0 + u < out) stage[fin + j0 + u] = x[u];
+  };
+  // the keys to scan: [0, S), or the chunks between the extreme valid entries
+  int64_t lo = 0, hi = (int64_t)S - 1;
+  if (S > 2ll * U.chunk) {
+    if (tid == 0) {
+      s_lo = INT32_MAX;
+      s_hi = -1;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kUThreads) src[i] = stage[i];
+    int mn = INT32_MAX, mx = -1;
+    for_entries([&](int32_t e, int) {
+      if (e >= 0 && e < S) {
+        mn = min(mn, e);
+        mx = max(mx, e);
+      }
+    });
+    mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if (lane == 0) {
+      atomicMin(&s_lo, mn);
+      atomicMax(&s_hi, mx);
+    }
+    __syncthreads();
+    lo = s_lo;
+    hi = s_hi;
   }
+  int nb = 0;  // union positions found so far
+  for (int64_t c0l = lo; c0l <= hi; c0l += U.chunk) {
+    const int c0 = (int)c0l;
+    const uint32_t span = (uint32_t)((c0l + U.chunk < (int64_t)S ? c0l + U.chunk : (int64_t)S) - c0l);
+    const int ng = (int)((span + 127) >> 7);  // 128-key groups (four words) of the chunk
+    for (int i = tid; i < ng; i += kUThreads) reinterpret_cast<uint4*>(bits)[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+    // 1. the bits of the chunk's valid entries
+    for_entries([&](int32_t e, int) {
+      const uint32_t o = (uint32_t)e - (uint32_t)c0;  // negative entries wrap past span
+      if (o < span) atomicOr(&bits[o >> 5], 1u << (o & 31));
+    });
+    __syncthreads();
+    // 2. the summary: bit g of word g / 32 when group g is not empty
+    for (int g0 = 32 * warp; g0 < ng; g0 += kUThreads) {
+      const int g = g0 + lane;
+      bool any = false;
+      if (g < ng) {
+        const uint4 v = reinterpret_cast<const uint4*>(bits)[g];
+        any = (v.x | v.y | v.z | v.w) != 0u;
+      }
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, any);
+      if (lane == 0) summary[g0 >> 5] = bal;
+    }
+    __syncthreads();
+    // thread t takes the summary bytes [t * per, (t + 1) * per) -- groups
+    // 8 * byte ... 8 * byte + 7 -- counts their bits, takes its prefix over
+    // the block, then writes the words' prefixes and the keys
+    const int nbytes = (ng + 7) >> 3;
+    const int per = (nbytes + kUThreads - 1) / kUThreads;
+    const int b0 = min(tid * per, nbytes), b1 = min(b0 + per, nbytes);
+    int cnt = 0;
+    for (int by = b0; by < b1; ++by) {
+      for (uint32_t s = (summary[by >> 2] >> (8 * (by & 3))) & 0xFFu; s; s &= s - 1) {
+        const uint4 v = reinterpret_cast<const uint4*>(bits)[8 * by + __ffs(s) - 1];
+        cnt += __popc(v.x) + __popc(v.y) + __popc(v.z) + __popc(v.w);
+      }
+    }
+    int n_chunk = 0;
+    int run = block_scan(cnt, &n_chunk, wtot);
+    for (int by = b0; by < b1; ++by) {
+      for (uint32_t s = (summary[by >> 2] >> (8 * (by & 3))) & 0xFFu; s; s &= s - 1) {
+        const int g = 8 * by + __ffs(s) - 1;
+        const uint4 v = reinterpret_cast<const uint4*>(bits)[g];
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t p[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          p[q] = (uint32_t)run;
+          int r = nb + run;
+          run += __popc(w4[q]);
+          const int k0 = c0 + 128 * g + 32 * q;
+          for (uint32_t m = w4[q]; m; m &= m - 1) keys[r++] = k0 + __ffs(m) - 1;
+        }
+        reinterpret_cast<uint2*>(pre)[g] = make_uint2(p[0] | p[1] << 16, p[2] | p[3] << 16);
+      }
+    }
+    __syncthreads();
+    // 3. each entry's rank, and its token's bit in that rank's mask
+    if (n_chunk * 4 <= U.m_bytes) {
+      for (int i = tid; i < n_chunk; i += kUThreads) m32[i] = 0u;
+      __syncthreads();
+      for_entries([&](int32_t e, int tok) {
+        const uint32_t o = (uint32_t)e - (uint32_t)c0;  // negative entries wrap past span
+        if (o < span) {
+          const int w = (int)(o >> 5);
+          const int r = pre[w] + __popc(bits[w] & ((1u << (o & 31)) - 1u));
+          atomicOr(&m32[r], 1u << tok);
+        }
+      });
+      __syncthreads();
+      for (int i = tid; i < n_chunk; i += kUThreads) masks[nb + i] = m32[i];
+      __syncthreads();
+    } else {
+      const int window = U.m_bytes / 16 * 8;  // 16-bit masks, two to a word
+      for (int w0 = 0; w0 < n_chunk; w0 += window) {
+        const int wn = min(window, n_chunk - w0);
+        for (int i = tid; i < (wn + 1) >> 1; i += kUThreads) m32[i] = 0u;
+        __syncthreads();
+        for_entries([&](int32_t e, int tok) {
+          const uint32_t o = (uint32_t)e - (uint32_t)c0;  // negative entries wrap past span
+          if (o < span) {
+            const int w = (int)(o >> 5);
+            const int r = pre[w] + __popc(bits[w] & ((1u << (o & 31)) - 1u)) - w0;
+            if (r >= 0 && r < wn) atomicOr(&m32[r >> 1], (1u << tok) << ((r & 1) << 4));
+          }
+        });
+        __syncthreads();
+        for (int i = tid; i < wn; i += kUThreads) masks[nb + w0 + i] = (m32[i >> 1] >> ((i & 1) << 4)) & 0xFFFFu;
+        __syncthreads();
+      }
+    }
+    nb += n_chunk;
+  }
+  if (tid == 0) *reinterpret_cast<int32_t*>(rec) = nb;
 }
 
 // ---------------------------------------------------------------------------
@@ -889,7 +942,6 @@ int check_attention_cfg(const dsa_attention_cfg* c) {
   return DSA_OK;
 }
 
-int union_smem(int G, int32_t Kc) { return (int)((int64_t)G * Kc * 4 + G * (kUBuckets + 1) * 2); }
 
 }  // namespace
 
@@ -915,21 +967,18 @@ int dsa_group_union(const dsa_attention_cfg* cfg, const int32_t* idx, void* work
   if (!idx || !workspace || (((uintptr_t)workspace) & 15u) || workspace_bytes < need) return DSA_ERR_INVALID_ARG;
   const int G = kRows / cfg->heads;
   const int groups = (cfg->tokens + G - 1) / G;
-  const int smem = union_smem(G, cfg->select);
+  const UnionShape U = union_shape(G, cfg->select, cfg->keys);
   static bool configured = false;
   if (!configured) {
-    const int most = (int)(kMaxUnionRows * 4 + kMaxUG * (kUBuckets + 1) * 2);
-    if (cudaFuncSetAttribute(union_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) != cudaSuccess ||
-        cudaFuncSetAttribute(union_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, most) != cudaSuccess) {
+    if (cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmemBudget) !=
+        cudaSuccess) {
       cudaGetLastError();
       return DSA_ERR_CUDA;
     }
     configured = true;
   }
-  auto* kern = G == 8 ? union_kernel<8> : union_kernel<16>;
-  kern<<<groups, kUThreads, smem, (cudaStream_t)stream>>>(idx, cfg->tokens, cfg->select, cfg->keys,
-                                                          static_cast<uint8_t*>(workspace),
-                                                          union_layout(G, cfg->select));
+  union_kernel<<<groups, kUThreads, U.smem, (cudaStream_t)stream>>>(
+      idx, cfg->tokens, cfg->select, cfg->keys, G, static_cast<uint8_t*>(workspace), union_layout(G, cfg->select), U);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -165,6 +165,68 @@ def test_widest_group_rows():
     _run(16, 16, 1 << 18, 6144, seed=6, own=0.3)
 
 
+def _union_only(idx, H, S):
+    # dsa_group_union alone against the oracle's union, every group
+    torch = _torch()
+    import sparse_attention_indexer_live_gb300 as dsa
+    T, Kc = idx.shape
+    G = 128 // H
+    cfg = dsa.dsa_attention_cfg(tokens=T, heads=H, keys=S, head_dim=128, value_dim=128, select=Kc)
+    ws = torch.full((dsa.dsa_sparse_attention_workspace(cfg),), 0x5A, dtype=torch.uint8, device="cuda:0")
+    dsa.dsa_group_union(cfg, torch.from_numpy(np.ascontiguousarray(idx)).to("cuda:0"), ws)
+    torch.cuda.synchronize()
+    groups = -(-T // G)
+    got = _union_from_ws(ws.cpu().numpy(), G, Kc, groups)
+    orc = oracle_default()
+    for g in range(groups):
+        keys, masks = orc.group_union(idx, g * G, G)
+        assert np.array_equal(got[g][0], keys), f"union keys of group {g}"
+        assert np.array_equal(got[g][1], masks), f"union masks of group {g}"
+
+
+def test_union_takes_rows_in_any_order():
+    # set semantics: shuffled rows, repeated entries and negative values other
+    # than -1 anywhere in a row give the oracle's union (16-byte and 4-byte
+    # entry loads)
+    rng = np.random.default_rng(14)
+    for T, H, S, Kc in ((40, 8, 5000, 64), (27, 16, 3001, 37)):
+        _, _, _, idx = wk.attention_inputs(T, H, S, Kc, seed=15, own=0.3, G=128 // H)
+        idx = idx.copy()
+        for t in range(T):
+            rng.shuffle(idx[t])
+        idx[rng.integers(0, T, 30), rng.integers(0, Kc, 30)] = -5
+        idx[rng.integers(0, T, 10), rng.integers(0, Kc, 10)] = np.iinfo(np.int32).min
+        rep = rng.integers(0, T, 40)
+        idx[rep, rng.integers(0, Kc, 40)] = idx[rep, rng.integers(0, Kc, 40)]
+        _union_only(idx, H, S)
+
+
+def _selections(T, S, Kc, seed, shared=0.5, lo=0):
+    # ascending distinct positions in [lo, lo + S) per token, a fraction
+    # `shared` of them common to the token's group of 16 (no key or value rows
+    # are made: the union alone is checked)
+    rng = np.random.default_rng(seed)
+    idx = np.full((T, Kc), -1, dtype=np.int32)
+    for g0 in range(0, T, 16):
+        base = rng.choice(S, size=int(shared * Kc), replace=False)
+        for t in range(g0, min(g0 + 16, T)):
+            own = rng.choice(S, size=Kc, replace=False)
+            sel = np.unique(np.concatenate([base, own]))[:Kc]
+            idx[t, :len(sel)] = np.sort(sel) + lo
+    return idx
+
+
+def test_union_over_several_key_chunks_and_mask_windows():
+    # 2^22 keys take several chunks of the key-space bitmap (and a first pass
+    # for the extreme entries); unions of ~40,000 positions take several
+    # windows of 16-bit masks
+    S = (1 << 22) + 12345
+    _union_only(_selections(32, S, 3072, seed=16, shared=0.2), 8, S)
+    # a narrow band of positions far into a huge key range: only the chunks
+    # between the smallest and largest entry are scanned
+    _union_only(_selections(16, 1 << 20, 512, seed=17, lo=1 << 30), 8, (1 << 31) - 1)
+
+
 def test_graph_replay_follows_new_selections():
     # both launches take their grids from the shapes only: a captured call
     # replays on new selections (written into the captured buffers) and gives
