@@ -289,9 +289,11 @@ __device__ void compact_best(uint64_t* buf, uint64_t* keep, int k, int cap, Shar
 
 // Ids of the set bits of bm among [0, nbits), ascending, into out[0 .. cap);
 // returns the number of set bits.  Each warp owns a contiguous run of words
-// and walks it 32 words at a time; for every non-zero word all 32 lanes write
-// that word's ids in parallel, so the cost does not depend on how the set bits
-// cluster.
+// and walks it 32 words at a time (lane = word).  A lane's position comes from
+// six ballots over the bit planes of the words' counts (no shuffle chain); a
+// word with one set bit is written by its own lane, and for every word with
+// more all 32 lanes write its ids in parallel, so the cost does not depend on
+// how the set bits cluster.
 template <typename OutT>
 __device__ int enumerate_bits(const uint32_t* bm, int64_t nbits, OutT* out, int cap, Shared& sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -325,25 +327,28 @@ __device__ int enumerate_bits(const uint32_t* bm, int64_t nbits, OutT* out, int 
   __syncthreads();
   int running = sh.warp_tot[warp];
   const int total = sh.warp_tot[kWarps];
+  const uint32_t lt = lanemask_lt();
   for (int c = w_begin; c < w_end; c += 32) {
     const uint32_t x = word(c + lane);
-    const int pc = __popc(x);
-    int incl = pc;
+    const uint32_t pc = (uint32_t)__popc(x);  // <= 32: six bit planes
+    int below = 0, tot = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(kFull, incl, o);
-      if (lane >= o) incl += y;
+    for (int b = 0; b < 6; ++b) {
+      const uint32_t plane = __ballot_sync(kFull, (pc >> b) & 1u);
+      below += __popc(plane & lt) << b;
+      tot += __popc(plane) << b;
     }
-    const int base = running + incl - pc;
-    running += __shfl_sync(kFull, incl, 31);
-    uint32_t nz = __ballot_sync(kFull, x != 0);
-    while (nz) {
-      const int j = __ffs(nz) - 1;
-      nz &= nz - 1;
+    const int base = running + below;
+    running += tot;
+    if (pc == 1u && base < cap) out[base] = (OutT)((c + lane) * 32 + __ffs(x) - 1);
+    uint32_t multi = __ballot_sync(kFull, pc > 1u);
+    while (multi) {
+      const int j = __ffs(multi) - 1;
+      multi &= multi - 1;
       const uint32_t xj = __shfl_sync(kFull, x, j);
       const int bj = __shfl_sync(kFull, base, j);
       if ((xj >> lane) & 1u) {
-        const int pos = bj + __popc(xj & lanemask_lt());
+        const int pos = bj + __popc(xj & lt);
         if (pos < cap) out[pos] = (OutT)((c + j) * 32 + lane);
       }
     }
