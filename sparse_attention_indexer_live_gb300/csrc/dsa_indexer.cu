@@ -251,10 +251,27 @@ __device__ __forceinline__ uint32_t okey(uint32_t u) { return u ^ ((uint32_t)((i
 // The fp32 bits whose order key is k.
 __device__ __forceinline__ uint32_t okey_inv(uint32_t k) { return (k & 0x80000000u) ? (k ^ 0x80000000u) : ~k; }
 
+// ReLU of a head score on the FMA pipe: 2^25 * sat(x * 2^-25), with the 2^25
+// folded into the head weight (kSatScale).  A score is a sum of 128 products
+// of e4m3 values, so it is 0, NaN (e4m3 NaN inputs) or of magnitude in
+// [2^-18, 128 * 448^2 < 2^25]: scaling by 2^-25 is exact and stays normal,
+// sat clamps negatives (and NaN) to +0, and (w * 2^25) * (x * 2^-25) is the
+// exact product w * x -- so the fused multiply-add that takes it rounds to
+// the same bits as with max(x, 0) and the unscaled weight.
+constexpr float kSatScale = 33554432.0f;  // 2^25
+__device__ __forceinline__ float relu_sat(uint32_t x) {
+  float d;
+  asm("mul.rn.sat.f32 %0, %1, 0f33000000;" : "=f"(d) : "f"(__uint_as_float(x)));  // x * 2^-25, clamped to [0, 1]
+  return d;
+}
+
 // One logit from this thread's TMEM lane: the query's 64 head scores in
 // 16-column chunks, weighted ReLU sum with two packed partial sums (heads 0,1
-// and 2,3 mod 4), times the key's scale.  Every mode uses this one routine, so
-// a key's logit has the same bits whichever launch computes it.
+// and 2,3 mod 4), times the key's scale.  Heads 0,1 mod 4 take the ReLU as a
+// max (ALU pipe), heads 2,3 mod 4 as relu_sat (FMA pipe; their weights in wr
+// carry the factor 2^25), which splits the per-element work between the two
+// pipes.  Every mode uses this one routine, so a key's logit has the same
+// bits whichever launch computes it.
 __device__ __forceinline__ float lane_logit(uint32_t col, const float4 (&wr)[kHeads / 4], float ksc) {
   uint64_t acc01 = 0ull, acc23 = 0ull;
   uint32_t r[16];
@@ -268,9 +285,7 @@ __device__ __forceinline__ float lane_logit(uint32_t col, const float4 (&wr)[kHe
       acc01 = ffma2(pack2(wv.x, wv.y),
                     pack2(fmaxf(__uint_as_float(r[4 * j + 0]), 0.f), fmaxf(__uint_as_float(r[4 * j + 1]), 0.f)),
                     acc01);
-      acc23 = ffma2(pack2(wv.z, wv.w),
-                    pack2(fmaxf(__uint_as_float(r[4 * j + 2]), 0.f), fmaxf(__uint_as_float(r[4 * j + 3]), 0.f)),
-                    acc23);
+      acc23 = ffma2(pack2(wv.z, wv.w), pack2(relu_sat(r[4 * j + 2]), relu_sat(r[4 * j + 3])), acc23);
     }
   }
   float acc0, acc1, acc2, acc3;
@@ -379,7 +394,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   for (int i = threadIdx.x; i < kQueriesPerCta * kHeads; i += kThreads) {
     const int q = i / kHeads;
-    ws[i] = q < nq ? p.w[(int64_t)(t0 + q) * kHeads + (i % kHeads)] : 0.f;
+    // heads 2,3 mod 4 carry relu_sat's factor 2^25 (exact: a power of two)
+    ws[i] = q < nq ? p.w[(int64_t)(t0 + q) * kHeads + (i % kHeads)] * ((i & 2) ? kSatScale : 1.0f) : 0.f;
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
