@@ -154,6 +154,9 @@ __global__ void __launch_bounds__(kUThreads)
   uint16_t* pre = reinterpret_cast<uint16_t*>(usm + U.pre_off);
   uint32_t* summary = reinterpret_cast<uint32_t*>(usm + U.sum_off);
   uint32_t* m32 = reinterpret_cast<uint32_t*>(usm + U.m_off);
+  // the attention launch that reads these records may start its own setup now
+  // (it waits for this grid to finish before reading them)
+  asm volatile("griddepcontrol.launch_dependents;");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int grp = blockIdx.x;
   const int t0 = grp * G;
@@ -599,11 +602,22 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   const int G = p.G;
   const int t0 = grp * G;
   const uint8_t* rec = p.ws + (int64_t)grp * p.L.bytes;
-  const int n = *reinterpret_cast<const int32_t*>(rec);
   const int32_t* ukeys = reinterpret_cast<const int32_t*>(rec + p.L.keys_off);
   const uint32_t* umasks = reinterpret_cast<const uint32_t*>(rec + p.L.masks_off);
-  const int ntiles = (n + kTileN - 1) / kTileN;
 
+  // warps 0-1 start the Q tile's copy at once: it does not depend on the union
+  if (warp < 2) {
+    const int half = lane >> 4, c = lane & 15;
+    const int wrow = 64 * warp;
+    for (int j = 0; j < 32; ++j) {
+      const int row = wrow + 2 * j + half;
+      const int64_t qr = (int64_t)t0 * p.H + row;  // query/head row
+      if (qr < (int64_t)p.T * p.H)
+        cp16(sb + kOffQ + sw_off(row, c), p.q + qr * kDim + 8 * c);
+      else
+        st16(sb + kOffQ + sw_off(row, c), make_uint4(0, 0, 0, 0));
+    }
+  }
   if (threadIdx.x == 0) {
     s_attn_abort = 0;
 #ifdef DSA_ATTENTION_TEST_STARVE
@@ -637,12 +651,19 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   __syncthreads();
   fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The union records come from the launch before this one, which may still
+  // be running (programmatic dependent launch: this grid's setup above and
+  // the Q copy overlap its end); wait for it to finish and its writes to be
+  // visible before the first read.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int n = *reinterpret_cast<const int32_t*>(rec);
+  const int ntiles = (n + kTileN - 1) / kTileN;
 
   if (warp < 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kLoadRegs));
     if (warp < 4) {
       // ---- loaders: warps 0-1 Q and K (2 stages), warps 2-3 V (3 stages).
-      // Warps 0-1 first copy the Q tile.  Then each warp of a pair loads
+      // Warps 0-1 first finish the Q tile's copy.  Then each warp of a pair loads
       // every other tile whole, so two tiles are in flight.  One copy
       // instruction moves two whole rows (a half-warp per 256-byte row, 16
       // bytes a lane), so every request is a full row; positions past the
@@ -656,16 +677,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
       uint64_t* empty = is_k ? kempty : vempty;
       const uint32_t tile_base = sb + (is_k ? kOffK : kOffV);
       if (is_k) {
-        const int wrow = 64 * warp;
-        for (int j = 0; j < 32; ++j) {
-          const int row = wrow + 2 * j + half;
-          const int64_t qr = (int64_t)t0 * p.H + row;  // query/head row
-          if (qr < (int64_t)p.T * p.H)
-            cp16(sb + kOffQ + sw_off(row, c), p.q + qr * kDim + 8 * c);
-          else
-            st16(sb + kOffQ + sw_off(row, c), make_uint4(0, 0, 0, 0));
-        }
-        cp_wait_all();
+        cp_wait_all();  // the Q copy issued at the start
         fence_async_smem();
         bar_arrive(qfull);
       }
@@ -1021,7 +1033,23 @@ int dsa_sparse_attention(const dsa_attention_cfg* cfg, const uint16_t* q, const 
   P.log2H = cfg->heads == 8 ? 3 : 4;
   P.G = G;
   P.scale_log2 = scale * 1.4426950408889634f;
-  attention_kernel<<<groups, kAThreads, kSmemA, (cudaStream_t)stream>>>(P);
+  // programmatic dependent launch: the kernel may begin while the union
+  // launch before it finishes, and waits for it before reading the records
+  cudaLaunchConfig_t lc;
+  memset(&lc, 0, sizeof(lc));
+  lc.gridDim = dim3((unsigned)groups);
+  lc.blockDim = dim3(kAThreads);
+  lc.dynamicSmemBytes = kSmemA;
+  lc.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  if (cudaLaunchKernelEx(&lc, attention_kernel, P) != cudaSuccess) {
+    cudaGetLastError();
+    return DSA_ERR_CUDA;
+  }
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
