@@ -468,6 +468,8 @@ EXTRAS = {
         dsa, torch, dev, T=96, S=1 << 20),
     "grouped_sparse_attention": lambda dsa, torch, dev, local, prefill: measure_attention(
         dsa, torch, dev),
+    "grouped_sparse_attention_ranges": lambda dsa, torch, dev, local, prefill: measure_attention_ranges(
+        dsa, torch, dev),
 }
 
 
@@ -553,6 +555,78 @@ def measure_fused(dsa, torch, dev, T=608, S=131072, B=8, Kb=256, K=2048):
     return res
 
 
+def _graph_timed(torch, f, reps=20):
+    """us per call of f, with reps calls captured in one CUDA graph: the replay
+    times the kernels, not the host's launch rate."""
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            f()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(reps):
+            f()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = _events(torch, 2)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def measure_attention_ranges(dsa, torch, dev, T=2048, H=8, Sr=1 << 20, blk=128, window=512):
+    """The range form of the grouped attention (dsa_sparse_attention_ranges)
+    on a compressed-prefix-plus-window selection: keys [0, Sc) hold one
+    compressed entry per `blk` positions, keys [Sc, Sc + Sr) the raw
+    positions; the T tokens are the last T positions of the context, and
+    token t at position p attends to the compressed entries [0, (p + 1) / blk)
+    and the raw window [p - window + 1, p] -- two ranges, no index lists."""
+    Sc = Sr // blk
+    S = Sc + Sr
+    q, k, v, _ = wk.attention_inputs(T, H, S, 8, seed=22, G=128 // H)
+    pos = Sr - T + np.arange(T)
+    ranges = np.zeros((T, 2, 2), dtype=np.int32)
+    ranges[:, 0, 1] = (pos + 1) // blk
+    ranges[:, 1, 0] = Sc + np.maximum(0, pos - window + 1)
+    ranges[:, 1, 1] = Sc + pos + 1
+    select = Sc + window
+    qd, kd, vd = (torch.from_numpy(x.view(np.int16)).to(dev) for x in (q, k, v))
+    rd = torch.from_numpy(ranges).to(dev)
+    cfg = dsa.ranges_attention_cfg(qd, kd, rd, select)
+    ws = torch.zeros(dsa.dsa_sparse_attention_ranges_workspace(cfg, 2), dtype=torch.uint8, device=dev)
+    o = torch.empty((T, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(128)
+    us_union = _graph_timed(torch, lambda: dsa.dsa_group_union_ranges(cfg, rd, ws))
+    us = _graph_timed(torch, lambda: dsa.dsa_sparse_attention_ranges(cfg, qd, kd, vd, rd, scale, ws, o, lse))
+    G = 128 // H
+    groups = -(-T // G)
+    cap = G * select
+    rec = 16 + 2 * ((cap * 4 + 15) & ~15)
+    wsn = ws.cpu().numpy()
+    union = np.array([int(wsn[g * rec:g * rec + 4].view(np.int32)[0]) for g in range(groups)])
+    sel = (ranges[:, :, 1] - ranges[:, :, 0]).sum(axis=1)
+    u_tot = float(union.sum())
+    union_bytes = 16.0 * T + groups * 16 + 8.0 * u_tot
+    attn_bytes = 4.0 + 8.0 * u_tot + T * H * 128 * 2 + 2 * 256 * u_tot + T * H * (128 * 4 + 4)
+    hbm, hbm_src = hbm_peak()
+    useful = 2.0 * H * float(sel.sum()) * (128 + 128)
+    us_attn = us - us_union
+    return {"tokens": T, "heads": H, "group": G, "keys": S, "compressed": Sc, "window": window,
+            "ranges_per_token": 2, "us_per_call": us, "us_union": us_union, "us_attention": us_attn,
+            "tokens_per_s": T / (us * 1e-6), "union_over_selection": float(union.mean() / sel.mean()),
+            "roofline": {"bound": "hbm", "unit": "GB/s", "peak": hbm, "peak_source": hbm_src,
+                         "bytes_per_call": union_bytes + attn_bytes,
+                         "achieved": (union_bytes + attn_bytes) / (us * 1e-6) / 1e9,
+                         "frac": (union_bytes + attn_bytes) / (us * 1e-6) / 1e9 / hbm,
+                         "attention_kernel_frac": attn_bytes / (us_attn * 1e-6) / 1e9 / hbm},
+            "useful_tflops": useful / (us * 1e-6) / 1e12, "status": dsa.dsa_sparse_attention_status()}
+
+
 def measure_attention(dsa, torch, dev, T=2048, H=8, S=1 << 20, Kc=2048, own=0.05):
     """Grouped masked sparse attention (dsa_sparse_attention): union build plus
     attention, on T tokens whose neighbours share most of their selection.
@@ -571,28 +645,7 @@ def measure_attention(dsa, torch, dev, T=2048, H=8, S=1 << 20, Kc=2048, own=0.05
     lse = torch.empty((T, H), dtype=torch.float32, device=dev)
     scale = 1.0 / math.sqrt(128)
 
-    def timed(f, reps=20):
-        # reps calls captured in one CUDA graph: the replay times the kernels,
-        # not the host's launch rate
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            for _ in range(3):
-                f()
-        s.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=s):
-            for _ in range(reps):
-                f()
-        g.replay()
-        torch.cuda.synchronize()
-        e0, e1 = _events(torch, 2)
-        e0.record()
-        g.replay()
-        e1.record()
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / reps
-
+    timed = lambda f: _graph_timed(torch, f)
     us_union = timed(lambda: dsa.dsa_group_union(cfg, idd, ws))
     us = timed(lambda: dsa.dsa_sparse_attention(cfg, qd, kd, vd, idd, scale, ws, o, lse))
     G = 128 // H

@@ -289,6 +289,41 @@ int dsa_sparse_attention(const dsa_attention_cfg* cfg, const uint16_t* q, const 
                          const uint16_t* v, const int32_t* idx, float scale, void* workspace,
                          size_t workspace_bytes, float* o, float* lse, struct CUstream_st* stream);
 
+/*
+ * The same attention when each token's selection is a set of position ranges
+ * instead of an index list: the structure-aware form of vLLM PR #48726
+ * ("LiteDSA: grouped masked sparse attention"), where DeepSeek-V4's C128A path
+ * represents its compressed prefix plus sliding window as exact per-query
+ * ranges over the group union, derived from positions, without materialising
+ * the [tokens, topk + window] combined index matrix.  The pages give no
+ * formula; this build's reading: token t attends to every key position in the
+ * union of its ranges, with the multi-query attention above.
+ *   ranges   int32 [tokens, nranges, 2]: half-open [lo, hi) key positions; an
+ *            empty range (lo >= hi) is ignored, positions outside [0, keys)
+ *            are dropped, overlapping ranges of a token count once
+ *   nranges  1 .. 8 ranges per token
+ *   cfg->select: the most positions the ranges of one token cover (sizes each
+ *            group's record: G * select <= 2^24; a group whose union exceeds
+ *            G * select is cut there)
+ *   workspace: dsa_sparse_attention_ranges_workspace() bytes, the record
+ *            layout of dsa_sparse_attention (union ascending, token masks)
+ * Errors: DSA_ERR_INVALID_ARG for a null or misaligned pointer, a workspace
+ * too small or nranges < 1; DSA_ERR_UNSUPPORTED for nranges > 8 or the
+ * shapes dsa_sparse_attention does not take.
+ */
+int dsa_sparse_attention_ranges_workspace(const dsa_attention_cfg* cfg, int32_t nranges, size_t* bytes);
+
+/* Only the unions and masks, into workspace (the first launch of
+ * dsa_sparse_attention_ranges). */
+int dsa_group_union_ranges(const dsa_attention_cfg* cfg, const int32_t* ranges, int32_t nranges, void* workspace,
+                           size_t workspace_bytes, struct CUstream_st* stream);
+
+/* The unions from ranges, then the attention of dsa_sparse_attention. */
+int dsa_sparse_attention_ranges(const dsa_attention_cfg* cfg, const uint16_t* q, const uint16_t* k,
+                                const uint16_t* v, const int32_t* ranges, int32_t nranges, float scale,
+                                void* workspace, size_t workspace_bytes, float* o, float* lse,
+                                struct CUstream_st* stream);
+
 /* DSA_ERR_TIMEOUT once after an attention launch gave up a wait (then
  * cleared), else DSA_OK; synchronises the device. */
 int dsa_sparse_attention_status(void);

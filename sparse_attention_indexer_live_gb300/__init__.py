@@ -5,6 +5,8 @@ The work runs in hand-written sm_103a CUDA kernels behind a C ABI
 Python binding over it.
 """
 from .binding import (attention_cfg, dsa_attention_cfg, dsa_group_union, dsa_sparse_attention,
+                      dsa_group_union_ranges, dsa_sparse_attention_ranges,
+                      dsa_sparse_attention_ranges_workspace, ranges_attention_cfg,
                       dsa_sparse_attention_status, dsa_sparse_attention_workspace, DSA_ERR_CUDA, DSA_ERR_INVALID_ARG, DSA_ERR_TIMEOUT, DSA_ERR_UNSUPPORTED,
                       DSA_OK, NOALLOC_SCRATCH_BYTES, DsaSelectError, EXPORTS, Plan,
                       dsa_candidate_select,
@@ -25,4 +27,5 @@ __all__ = ["DSA_OK", "DSA_ERR_INVALID_ARG", "DSA_ERR_UNSUPPORTED", "DSA_ERR_CUDA
            "dsa_indexer_status", "status_string", "load", "build", "LIB_PATH",
            "Shard", "ShardedSelector", "shard_rows", "attention_cfg", "dsa_attention_cfg",
            "dsa_group_union", "dsa_sparse_attention_workspace", "dsa_sparse_attention",
-           "dsa_sparse_attention_status"]
+           "dsa_sparse_attention_status", "ranges_attention_cfg", "dsa_sparse_attention_ranges_workspace",
+           "dsa_group_union_ranges", "dsa_sparse_attention_ranges"]

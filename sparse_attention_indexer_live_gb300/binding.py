@@ -39,7 +39,8 @@ EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_ca
            "dsa_row_topk", "dsa_select_topk", "dsa_combine_window", "dsa_indexer_logits",
            "dsa_indexer_status", "dsa_indexer_select_workspace", "dsa_indexer_select",
            "dsa_indexer_select_noalloc", "dsa_sparse_attention_workspace", "dsa_group_union",
-           "dsa_sparse_attention", "dsa_sparse_attention_status", "dsa_status_string")
+           "dsa_sparse_attention", "dsa_sparse_attention_ranges_workspace", "dsa_group_union_ranges",
+           "dsa_sparse_attention_ranges", "dsa_sparse_attention_status", "dsa_status_string")
 
 # Size of the library's fixed scratch array used by dsa_indexer_select_noalloc
 # (DSA_NOALLOC_SCRATCH_BYTES in include/dsa_select.h).
@@ -109,6 +110,15 @@ def load(path: str | None = None):
             L.dsa_sparse_attention.restype = i32
             L.dsa_sparse_attention.argtypes = [ctypes.POINTER(dsa_attention_cfg), vp, vp, vp, vp,
                                                ctypes.c_float, vp, ctypes.c_size_t, vp, vp, vp]
+            L.dsa_sparse_attention_ranges_workspace.restype = i32
+            L.dsa_sparse_attention_ranges_workspace.argtypes = [ctypes.POINTER(dsa_attention_cfg), i32,
+                                                                ctypes.POINTER(ctypes.c_size_t)]
+            L.dsa_group_union_ranges.restype = i32
+            L.dsa_group_union_ranges.argtypes = [ctypes.POINTER(dsa_attention_cfg), vp, i32, vp,
+                                                 ctypes.c_size_t, vp]
+            L.dsa_sparse_attention_ranges.restype = i32
+            L.dsa_sparse_attention_ranges.argtypes = [ctypes.POINTER(dsa_attention_cfg), vp, vp, vp, vp, i32,
+                                                      ctypes.c_float, vp, ctypes.c_size_t, vp, vp, vp]
             L.dsa_sparse_attention_status.restype = i32
             L.dsa_sparse_attention_status.argtypes = []
             L.dsa_indexer_select_noalloc.restype = i32
@@ -431,6 +441,61 @@ def dsa_sparse_attention(cfg: dsa_attention_cfg, q, k, v, idx, scale: float, wor
     _check(load().dsa_sparse_attention(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(idx),
                                        float(scale), _ptr(workspace), workspace.numel(), _ptr(o),
                                        _ptr(lse), _stream(stream)), "dsa_sparse_attention")
+
+
+def ranges_attention_cfg(q, k, ranges, select: int) -> dsa_attention_cfg:
+    """cfg of the range form: `select` bounds the positions one token's ranges
+    cover."""
+    T, H, D = q.shape
+    return dsa_attention_cfg(tokens=T, heads=H, keys=k.shape[0], head_dim=D, value_dim=D,
+                             select=int(select))
+
+
+def dsa_sparse_attention_ranges_workspace(cfg: dsa_attention_cfg, nranges: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load().dsa_sparse_attention_ranges_workspace(ctypes.byref(cfg), int(nranges), ctypes.byref(n)),
+           "dsa_sparse_attention_ranges_workspace")
+    return int(n.value)
+
+
+def _attention_ranges(cfg: dsa_attention_cfg, ranges, workspace) -> int:
+    import torch
+    if ranges.dim() != 3 or ranges.shape[2] != 2:
+        raise ValueError(f"ranges must be [tokens, nranges, 2], got {tuple(ranges.shape)}")
+    if ranges.shape[0] != max(cfg.tokens, 0):
+        raise ValueError(f"ranges has {ranges.shape[0]} tokens, cfg.tokens = {cfg.tokens}")
+    _i32("ranges", ranges, max(cfg.tokens, 0) * ranges.shape[1] * 2)
+    _tensor("workspace", workspace, (torch.uint8,), device=ranges.device.index)
+    return int(ranges.shape[1])
+
+
+def dsa_group_union_ranges(cfg: dsa_attention_cfg, ranges, workspace, stream=None):
+    """The unions of each group's position ranges and their token masks,
+    written to workspace (the record layout of dsa_group_union)."""
+    nr = _attention_ranges(cfg, ranges, workspace)
+    _check(load().dsa_group_union_ranges(ctypes.byref(cfg), _ptr(ranges), nr, _ptr(workspace),
+                                         workspace.numel(), _stream(stream)), "dsa_group_union_ranges")
+
+
+def dsa_sparse_attention_ranges(cfg: dsa_attention_cfg, q, k, v, ranges, scale: float, workspace, o, lse,
+                                stream=None):
+    """Grouped masked sparse attention over per-token position ranges:
+    ranges [T, nranges, 2] int32 half-open [lo, hi); otherwise as
+    dsa_sparse_attention."""
+    import torch
+    nr = _attention_ranges(cfg, ranges, workspace)
+    dev = ranges.device.index
+    T, H, S = max(cfg.tokens, 0), max(cfg.heads, 0), max(cfg.keys, 0)
+    D, Dv = max(cfg.head_dim, 0), max(cfg.value_dim, 0)
+    half = (torch.bfloat16, torch.uint16, torch.int16)
+    _tensor("q", q, half, numel=T * H * D, device=dev)
+    _tensor("k", k, half, numel=S * D, device=dev)
+    _tensor("v", v, half, numel=S * Dv, device=dev)
+    _tensor("o", o, (torch.float32,), numel=T * H * Dv, device=dev)
+    _tensor("lse", lse, (torch.float32,), numel=T * H, device=dev)
+    _check(load().dsa_sparse_attention_ranges(ctypes.byref(cfg), _ptr(q), _ptr(k), _ptr(v), _ptr(ranges), nr,
+                                              float(scale), _ptr(workspace), workspace.numel(), _ptr(o),
+                                              _ptr(lse), _stream(stream)), "dsa_sparse_attention_ranges")
 
 
 def dsa_sparse_attention_status() -> int:

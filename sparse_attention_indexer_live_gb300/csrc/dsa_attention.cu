@@ -322,6 +322,144 @@ __global__ void __launch_bounds__(kUThreads)
 }
 
 // ---------------------------------------------------------------------------
+// union from position ranges (the structure-aware form)
+
+constexpr int kRThreads = 512;
+constexpr int kMaxRanges = 8;                         // ranges per token
+constexpr int kMaxIv = 16 * kMaxRanges;               // a group's ranges (G <= 16)
+constexpr int kMaxEv = 2 * kMaxIv;                    // their end points
+constexpr int64_t kMaxRangeUnion = (int64_t)1 << 24;  // G * select in the range form
+static_assert(kMaxEv <= kRThreads, "one thread per end point ranks the group's end points");
+
+// Union of one group's selections when each token's selection is given as up
+// to R half-open position ranges [lo, hi) (vLLM PR #48726, "LiteDSA: grouped
+// masked sparse attention": DeepSeek-V4's C128A path represents its
+// compressed prefix plus sliding window as exact per-query ranges over the
+// group union, derived from positions, without the combined index matrix).
+//   1. the ranges, clamped to [0, S); each token's own merged (one thread per
+//      token), so that a token's ranges are disjoint and ascending;
+//   2. their end points ranked by position (one thread each);
+//   3. one sweep over the sorted end points (thread 0) cuts the union into
+//      segments between consecutive end points, each with a constant mask of
+//      the tokens covering it (a token's bit flips at each of its end
+//      points), and gives each covered segment its first union index;
+//   4. every thread writes union positions: the segment by a binary search
+//      over those indices, the key and the segment's mask -- the record the
+//      attention reads for an index-list selection.
+// At most `cap` positions are written (the union of G tokens' ranges, each
+// covering at most `select` positions, fits).
+__global__ void __launch_bounds__(kRThreads)
+    range_union_kernel(const int32_t* ranges, int32_t T, int32_t R, int32_t S, int32_t G, uint8_t* ws,
+                       UnionLayout L, int64_t cap) {
+  __shared__ int2 iv[kMaxIv];            // token g's ranges at [g R, g R + R); empty = (0, 0)
+  __shared__ int2 ev[kMaxEv];            // end points (position, token); unused = (INT32_MAX, 0)
+  __shared__ int2 evs[kMaxEv];           // the same, by position
+  __shared__ int32_t seg_lo[kMaxEv];     // covered segments: first key, token mask, first union index
+  __shared__ uint32_t seg_mask[kMaxEv];
+  __shared__ int64_t seg_off[kMaxEv + 1];
+  __shared__ int s_nseg;
+  // the attention launch that reads these records may start its own setup now
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int grp = blockIdx.x;
+  const int t0 = grp * G;
+  const int nt = min(G, T - t0);
+  const int nr = nt * R;
+  uint8_t* rec = ws + (int64_t)grp * L.bytes;
+  int32_t* keys = reinterpret_cast<int32_t*>(rec + L.keys_off);
+  uint32_t* masks = reinterpret_cast<uint32_t*>(rec + L.masks_off);
+  for (int i = threadIdx.x; i < nr; i += kRThreads) {
+    const int32_t* rp = ranges + ((int64_t)t0 * R + i) * 2;
+    int lo = max(rp[0], 0), hi = min(rp[1], S);
+    if (hi <= lo) lo = hi = 0;
+    iv[i] = make_int2(lo, hi);
+  }
+  __syncthreads();
+  // 1. a token's ranges: sorted by start, overlapping or touching ones merged
+  if (threadIdx.x < nt) {
+    int2* t = iv + threadIdx.x * R;
+    for (int i = 1; i < R; ++i) {  // insertion sort, empty ranges last
+      const int2 x = t[i];
+      const bool xe = x.y <= x.x;
+      int j = i - 1;
+      while (j >= 0) {
+        const bool te = t[j].y <= t[j].x;
+        if (!(te && !xe) && (xe || t[j].x <= x.x)) break;
+        t[j + 1] = t[j];
+        --j;
+      }
+      t[j + 1] = x;
+    }
+    int m = 0;
+    for (int i = 0; i < R; ++i) {
+      const int2 x = t[i];
+      if (x.y <= x.x) break;
+      if (m > 0 && x.x <= t[m - 1].y) {
+        t[m - 1].y = max(t[m - 1].y, x.y);
+      } else {
+        t[m++] = x;
+      }
+    }
+    for (int i = m; i < R; ++i) t[i] = make_int2(0, 0);
+  }
+  __syncthreads();
+  // 2. the end points, ranked by (position, slot)
+  const int ne = 2 * nr;
+  if (threadIdx.x < ne) {
+    const int2 x = iv[threadIdx.x >> 1];
+    ev[threadIdx.x] = x.y > x.x ? make_int2((threadIdx.x & 1) ? x.y : x.x, (threadIdx.x >> 1) / R)
+                                : make_int2(INT32_MAX, 0);
+  }
+  __syncthreads();
+  if (threadIdx.x < ne) {
+    const int k = threadIdx.x;
+    const int2 a = ev[k];
+    int rank = 0;
+    for (int j = 0; j < ne; ++j) {
+      const int2 b = ev[j];
+      rank += b.x < a.x || (b.x == a.x && j < k);
+    }
+    evs[rank] = a;
+  }
+  __syncthreads();
+  // 3. the sweep
+  if (threadIdx.x == 0) {
+    uint32_t mask = 0;
+    int nseg = 0;
+    int64_t u = 0;
+    int prev = 0;
+    for (int k = 0; k < ne; ++k) {
+      const int2 e = evs[k];
+      if (e.x == INT32_MAX) break;
+      if (mask != 0 && e.x > prev) {
+        seg_lo[nseg] = prev;
+        seg_mask[nseg] = mask;
+        seg_off[nseg] = u;
+        u += e.x - prev;
+        ++nseg;
+      }
+      mask ^= 1u << e.y;
+      prev = e.x;
+    }
+    seg_off[nseg] = u;
+    s_nseg = nseg;
+  }
+  __syncthreads();
+  const int nseg = s_nseg;
+  const int64_t U = min(seg_off[nseg], cap);
+  if (threadIdx.x == 0) *reinterpret_cast<int32_t*>(rec) = (int32_t)U;
+  // 4. the union positions
+  for (int64_t u = threadIdx.x; u < U; u += kRThreads) {
+    int a = 0, b = nseg - 1;  // the last segment whose first index is <= u
+    while (a < b) {
+      const int c = (a + b + 1) >> 1;
+      if (seg_off[c] <= u) a = c; else b = c - 1;
+    }
+    keys[u] = seg_lo[a] + (int32_t)(u - seg_off[a]);
+    masks[u] = seg_mask[a];
+  }
+}
+
+// ---------------------------------------------------------------------------
 // attention
 
 constexpr int kAThreads = 512;  // warps 0-1 Q/K loaders, 2-3 V loaders, 4 MMA, 5 masks, 6-7 idle, 8-15 softmax
@@ -944,62 +1082,30 @@ __global__ void __launch_bounds__(kAThreads, 1) attention_kernel(const AttnParam
   }
 }
 
-// Shapes this build supports; DSA_OK when the call can run.
-int check_attention_cfg(const dsa_attention_cfg* c) {
+// Shapes this build supports; DSA_OK when the call can run.  max_union: the
+// largest G * select of the form (index lists: the union kernel's shared
+// memory; ranges: a bound on the record).
+int check_attention_cfg(const dsa_attention_cfg* c, int64_t max_union = kMaxUnionRows) {
   if (!c) return DSA_ERR_INVALID_ARG;
   if (c->tokens < 0 || c->keys < 0 || c->select < 0) return DSA_ERR_INVALID_ARG;
   if (c->heads != 8 && c->heads != 16) return DSA_ERR_UNSUPPORTED;
   if (c->head_dim != 128 || c->value_dim != 128) return DSA_ERR_UNSUPPORTED;
-  if ((int64_t)(kRows / c->heads) * c->select > kMaxUnionRows) return DSA_ERR_UNSUPPORTED;
+  if ((int64_t)(kRows / c->heads) * c->select > max_union) return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
 }
 
-
-}  // namespace
-
-extern "C" {
-
-int dsa_sparse_attention_workspace(const dsa_attention_cfg* cfg, size_t* bytes) {
-  if (!bytes) return DSA_ERR_INVALID_ARG;
-  *bytes = 0;
-  const int st = check_attention_cfg(cfg);
+int check_range_cfg(const dsa_attention_cfg* c, int32_t nranges) {
+  const int st = check_attention_cfg(c, kMaxRangeUnion);
   if (st != DSA_OK) return st;
-  const int G = kRows / cfg->heads;
-  const int64_t groups = ((int64_t)cfg->tokens + G - 1) / G;
-  *bytes = (size_t)(groups * union_layout(G, cfg->select).bytes);
+  if (nranges < 1) return DSA_ERR_INVALID_ARG;
+  if (nranges > kMaxRanges) return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
 }
 
-int dsa_group_union(const dsa_attention_cfg* cfg, const int32_t* idx, void* workspace, size_t workspace_bytes,
-                    struct CUstream_st* stream) {
-  size_t need = 0;
-  int st = dsa_sparse_attention_workspace(cfg, &need);
-  if (st != DSA_OK) return st;
-  if (cfg->tokens == 0) return DSA_OK;
-  if (!idx || !workspace || (((uintptr_t)workspace) & 15u) || workspace_bytes < need) return DSA_ERR_INVALID_ARG;
-  const int G = kRows / cfg->heads;
-  const int groups = (cfg->tokens + G - 1) / G;
-  const UnionShape U = union_shape(G, cfg->select, cfg->keys);
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmemBudget) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return DSA_ERR_CUDA;
-    }
-    configured = true;
-  }
-  union_kernel<<<groups, kUThreads, U.smem, (cudaStream_t)stream>>>(
-      idx, cfg->tokens, cfg->select, cfg->keys, G, static_cast<uint8_t*>(workspace), union_layout(G, cfg->select), U);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
-}
-
-int dsa_sparse_attention(const dsa_attention_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                         const int32_t* idx, float scale, void* workspace, size_t workspace_bytes, float* o,
-                         float* lse, struct CUstream_st* stream) {
-  int st = dsa_group_union(cfg, idx, workspace, workspace_bytes, stream);
-  if (st != DSA_OK) return st;
-  if (cfg->tokens == 0) return DSA_OK;
+// The attention over the records in `workspace` (written by the launch just
+// before on `stream`).
+int launch_attention(const dsa_attention_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                     float scale, void* workspace, float* o, float* lse, struct CUstream_st* stream) {
   if (!q || !o || !lse || (cfg->keys > 0 && (!k || !v))) return DSA_ERR_INVALID_ARG;
   if ((((uintptr_t)q) | ((uintptr_t)k) | ((uintptr_t)v) | ((uintptr_t)o)) & 15u) return DSA_ERR_INVALID_ARG;
   const int G = kRows / cfg->heads;
@@ -1051,6 +1157,91 @@ int dsa_sparse_attention(const dsa_attention_cfg* cfg, const uint16_t* q, const 
     return DSA_ERR_CUDA;
   }
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+
+}  // namespace
+
+extern "C" {
+
+int dsa_sparse_attention_workspace(const dsa_attention_cfg* cfg, size_t* bytes) {
+  if (!bytes) return DSA_ERR_INVALID_ARG;
+  *bytes = 0;
+  const int st = check_attention_cfg(cfg);
+  if (st != DSA_OK) return st;
+  const int G = kRows / cfg->heads;
+  const int64_t groups = ((int64_t)cfg->tokens + G - 1) / G;
+  *bytes = (size_t)(groups * union_layout(G, cfg->select).bytes);
+  return DSA_OK;
+}
+
+int dsa_group_union(const dsa_attention_cfg* cfg, const int32_t* idx, void* workspace, size_t workspace_bytes,
+                    struct CUstream_st* stream) {
+  size_t need = 0;
+  int st = dsa_sparse_attention_workspace(cfg, &need);
+  if (st != DSA_OK) return st;
+  if (cfg->tokens == 0) return DSA_OK;
+  if (!idx || !workspace || (((uintptr_t)workspace) & 15u) || workspace_bytes < need) return DSA_ERR_INVALID_ARG;
+  const int G = kRows / cfg->heads;
+  const int groups = (cfg->tokens + G - 1) / G;
+  const UnionShape U = union_shape(G, cfg->select, cfg->keys);
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(union_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kUSmemBudget) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return DSA_ERR_CUDA;
+    }
+    configured = true;
+  }
+  union_kernel<<<groups, kUThreads, U.smem, (cudaStream_t)stream>>>(
+      idx, cfg->tokens, cfg->select, cfg->keys, G, static_cast<uint8_t*>(workspace), union_layout(G, cfg->select), U);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_sparse_attention(const dsa_attention_cfg* cfg, const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                         const int32_t* idx, float scale, void* workspace, size_t workspace_bytes, float* o,
+                         float* lse, struct CUstream_st* stream) {
+  int st = dsa_group_union(cfg, idx, workspace, workspace_bytes, stream);
+  if (st != DSA_OK) return st;
+  if (cfg->tokens == 0) return DSA_OK;
+  return launch_attention(cfg, q, k, v, scale, workspace, o, lse, stream);
+}
+
+int dsa_sparse_attention_ranges_workspace(const dsa_attention_cfg* cfg, int32_t nranges, size_t* bytes) {
+  if (!bytes) return DSA_ERR_INVALID_ARG;
+  *bytes = 0;
+  const int st = check_range_cfg(cfg, nranges);
+  if (st != DSA_OK) return st;
+  const int G = kRows / cfg->heads;
+  const int64_t groups = ((int64_t)cfg->tokens + G - 1) / G;
+  *bytes = (size_t)(groups * union_layout(G, cfg->select).bytes);
+  return DSA_OK;
+}
+
+int dsa_group_union_ranges(const dsa_attention_cfg* cfg, const int32_t* ranges, int32_t nranges, void* workspace,
+                           size_t workspace_bytes, struct CUstream_st* stream) {
+  size_t need = 0;
+  int st = dsa_sparse_attention_ranges_workspace(cfg, nranges, &need);
+  if (st != DSA_OK) return st;
+  if (cfg->tokens == 0) return DSA_OK;
+  if (!ranges || !workspace || (((uintptr_t)workspace) & 15u) || workspace_bytes < need) return DSA_ERR_INVALID_ARG;
+  const int G = kRows / cfg->heads;
+  const int groups = (cfg->tokens + G - 1) / G;
+  range_union_kernel<<<groups, kRThreads, 0, (cudaStream_t)stream>>>(
+      ranges, cfg->tokens, nranges, cfg->keys, G, static_cast<uint8_t*>(workspace), union_layout(G, cfg->select),
+      (int64_t)G * cfg->select);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int dsa_sparse_attention_ranges(const dsa_attention_cfg* cfg, const uint16_t* q, const uint16_t* k,
+                                const uint16_t* v, const int32_t* ranges, int32_t nranges, float scale,
+                                void* workspace, size_t workspace_bytes, float* o, float* lse,
+                                struct CUstream_st* stream) {
+  int st = dsa_group_union_ranges(cfg, ranges, nranges, workspace, workspace_bytes, stream);
+  if (st != DSA_OK) return st;
+  if (cfg->tokens == 0) return DSA_OK;
+  return launch_attention(cfg, q, k, v, scale, workspace, o, lse, stream);
 }
 
 int dsa_sparse_attention_status(void) {

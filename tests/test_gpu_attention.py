@@ -227,6 +227,82 @@ def test_union_over_several_key_chunks_and_mask_windows():
     _union_only(_selections(16, 1 << 20, 512, seed=17, lo=1 << 30), 8, (1 << 31) - 1)
 
 
+def _expand_ranges(ranges, S):
+    # each token's positions: the union of its ranges clipped to [0, S),
+    # ascending, then -1 padding (the index-list form the oracle takes)
+    sets = []
+    for t in range(ranges.shape[0]):
+        pos = set()
+        for lo, hi in ranges[t]:
+            pos.update(range(max(int(lo), 0), min(int(hi), S)))
+        sets.append(sorted(pos))
+    width = max(1, max(len(x) for x in sets))
+    idx = np.full((ranges.shape[0], width), -1, dtype=np.int32)
+    for t, x in enumerate(sets):
+        idx[t, :len(x)] = x
+    return idx
+
+
+def _run_ranges(T, H, S, ranges, select, seed, scale=None):
+    torch = _torch()
+    import sparse_attention_indexer_live_gb300 as dsa
+    q, k, v, _ = wk.attention_inputs(T, H, S, 8, seed=seed, G=128 // H)
+    idx = _expand_ranges(ranges, S)
+    assert idx.shape[1] <= select or not (idx >= 0).any()
+    dev = "cuda:0"
+    qd, kd, vd = (torch.from_numpy(x.view(np.int16)).to(dev) for x in (q, k, v))
+    rd = torch.from_numpy(np.ascontiguousarray(ranges, dtype=np.int32)).to(dev)
+    cfg = dsa.ranges_attention_cfg(qd, kd, rd, select)
+    ws = torch.full((dsa.dsa_sparse_attention_ranges_workspace(cfg, ranges.shape[1]),), 0x5A,
+                    dtype=torch.uint8, device=dev)
+    o = torch.full((T, H, 128), 7.0, dtype=torch.float32, device=dev)
+    lse = torch.full((T, H), 7.0, dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(128) if scale is None else scale
+    dsa.dsa_sparse_attention_ranges(cfg, qd, kd, vd, rd, scale, ws, o, lse)
+    torch.cuda.synchronize()
+    assert dsa.dsa_sparse_attention_status() == dsa.DSA_OK
+    orc = oracle_default()
+    G = 128 // H
+    groups = -(-T // G)
+    got = _union_from_ws(ws.cpu().numpy(), G, select, groups)
+    for g in range(groups):
+        keys, masks = orc.group_union(idx, g * G, G)
+        assert np.array_equal(got[g][0], keys), f"union keys of group {g}"
+        assert np.array_equal(got[g][1], masks), f"union masks of group {g}"
+    o_ref, lse_ref = orc.sparse_attention(q, k, v, idx, scale)
+    _assert_within_bounds(idx, v, o.cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64),
+                          o_ref, lse_ref)
+
+
+def test_ranges_compressed_prefix_and_window():
+    # the C128A shape the pages describe: keys [0, Sc) are the compressed
+    # prefix (one entry per 128 positions), keys [Sc, Sc + Sr) the raw
+    # positions; token t at position p attends to the compressed entries of
+    # the blocks before it and to a sliding window of the last w raw positions
+    Sr, w, blk = 4096, 256, 128
+    Sc = Sr // blk
+    T, H = 40, 8
+    pos = 3000 + np.arange(T)
+    ranges = np.zeros((T, 2, 2), dtype=np.int32)
+    ranges[:, 0, 1] = (pos + 1) // blk
+    ranges[:, 1, 0] = Sc + np.maximum(0, pos - w + 1)
+    ranges[:, 1, 1] = Sc + pos + 1
+    _run_ranges(T, H, Sc + Sr, ranges, select=Sc + w, seed=18)
+
+
+def test_ranges_overlapping_empty_and_clipped():
+    # three ranges a token, some overlapping each other or a neighbour's,
+    # some empty or reversed, some reaching below 0 or past S; 16 heads
+    rng = np.random.default_rng(19)
+    T, H, S = 27, 16, 3000
+    lo = rng.integers(-200, S, size=(T, 3))
+    ln = rng.integers(-50, 400, size=(T, 3))
+    ranges = np.stack([lo, lo + ln], axis=2).astype(np.int32)
+    ranges[5] = [[10, 10], [200, 100], [-30, -1]]  # nothing selected
+    ranges[6] = [[S - 5, S + 50], [0, 3], [1, 2]]  # the first and last keys
+    _run_ranges(T, H, S, ranges, select=3 * 450, seed=20)
+
+
 def test_graph_replay_follows_new_selections():
     # both launches take their grids from the shapes only: a captured call
     # replays on new selections (written into the captured buffers) and gives
