@@ -126,6 +126,36 @@ def test_attention_arguments():
                          dev(torch.zeros(64, dtype=torch.int8)))
 
 
+def test_attention_range_arguments():
+    cfg = B.dsa_attention_cfg(tokens=4, heads=8, keys=100, head_dim=128, value_dim=128, select=16)
+    ws = dev(torch.zeros(64, dtype=torch.uint8))
+    assert B._attention_ranges(cfg, dev(torch.zeros(4, 2, 2, dtype=torch.int32)), ws) == 2
+    for shape in ((4, 2), (4, 2, 3), (3, 2, 2)):
+        with pytest.raises(ValueError):
+            B._attention_ranges(cfg, dev(torch.zeros(*shape, dtype=torch.int32)), ws)
+    with pytest.raises(TypeError):
+        B._attention_ranges(cfg, dev(torch.zeros(4, 2, 2, dtype=torch.int64)), ws)
+
+
+def test_attention_range_workspace_limits():
+    # the C ABI's own checks (no device call): 1..8 ranges a token, and a
+    # record bound far above the index-list form's
+    cfg = B.dsa_attention_cfg(tokens=2048, heads=8, keys=1 << 20, head_dim=128, value_dim=128,
+                              select=8704)
+    n = B.dsa_sparse_attention_ranges_workspace(cfg, 2)
+    G, cap = 16, 16 * 8704
+    assert n == 128 * (16 + 2 * ((cap * 4 + 15) & ~15))
+    for nr, status in ((0, B.DSA_ERR_INVALID_ARG), (9, B.DSA_ERR_UNSUPPORTED)):
+        with pytest.raises(B.DsaSelectError) as e:
+            B.dsa_sparse_attention_ranges_workspace(cfg, nr)
+        assert e.value.status == status
+    # the index-list form refuses this select (its union is built in shared memory)
+    with pytest.raises(B.DsaSelectError) as e:
+        B.dsa_sparse_attention_workspace(cfg)
+    assert e.value.status == B.DSA_ERR_UNSUPPORTED
+    del G
+
+
 def test_checks_survive_python_O():
     # under -O every assert statement is stripped; the checks must still raise
     code = ("import sys, torch; sys.path.insert(0, %r)\n"

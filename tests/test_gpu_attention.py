@@ -303,6 +303,50 @@ def test_ranges_overlapping_empty_and_clipped():
     _run_ranges(T, H, S, ranges, select=3 * 450, seed=20)
 
 
+def test_ranges_graph_replay_follows_new_ranges():
+    # the range form captured once replays on new ranges written into the
+    # captured buffer, and gives what a direct call gives
+    torch = _torch()
+    import sparse_attention_indexer_live_gb300 as dsa
+    T, H, S = 33, 8, 5000
+    q, k, v, _ = wk.attention_inputs(T, H, S, 8, seed=23)
+    rng = np.random.default_rng(24)
+
+    def ranges():
+        lo = rng.integers(0, S, size=(T, 2))
+        return np.stack([lo, lo + rng.integers(0, 300, size=(T, 2))], axis=2).astype(np.int32)
+
+    dev = "cuda:0"
+    qd, kd, vd = (torch.from_numpy(x.view(np.int16)).to(dev) for x in (q, k, v))
+    r0 = ranges()
+    rd = torch.from_numpy(r0).to(dev)
+    cfg = dsa.ranges_attention_cfg(qd, kd, rd, 600)
+    ws = torch.zeros(dsa.dsa_sparse_attention_ranges_workspace(cfg, 2), dtype=torch.uint8, device=dev)
+    o = torch.empty((T, H, 128), dtype=torch.float32, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(128)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        dsa.dsa_sparse_attention_ranges(cfg, qd, kd, vd, rd, scale, ws, o, lse, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        dsa.dsa_sparse_attention_ranges(cfg, qd, kd, vd, rd, scale, ws, o, lse, stream=stream)
+    for sel in (ranges(), r0):
+        rd.copy_(torch.from_numpy(sel))
+        graph.replay()
+        torch.cuda.synchronize()
+        og, lg = o.clone(), lse.clone()
+        dsa.dsa_sparse_attention_ranges(cfg, qd, kd, vd, rd, scale, ws, o, lse)
+        torch.cuda.synchronize()
+        assert torch.equal(og, o) and torch.equal(lg, lse)
+    assert dsa.dsa_sparse_attention_status() == dsa.DSA_OK
+    idx = _expand_ranges(r0, S)
+    o_ref, lse_ref = oracle_default().sparse_attention(q, k, v, idx, scale)
+    _assert_within_bounds(idx, v, og.cpu().numpy().astype(np.float64), lg.cpu().numpy().astype(np.float64),
+                          o_ref, lse_ref)
+
+
 def test_graph_replay_follows_new_selections():
     # both launches take their grids from the shapes only: a captured call
     # replays on new selections (written into the captured buffers) and gives
