@@ -339,13 +339,14 @@ static_assert(kMaxEv <= kRThreads, "one thread per end point ranks the group's e
 //   1. the ranges, clamped to [0, S); each token's own merged (one thread per
 //      token), so that a token's ranges are disjoint and ascending;
 //   2. their end points ranked by position (one thread each);
-//   3. one sweep over the sorted end points (thread 0) cuts the union into
-//      segments between consecutive end points, each with a constant mask of
-//      the tokens covering it (a token's bit flips at each of its end
-//      points), and gives each covered segment its first union index;
-//   4. every thread writes union positions: the segment by a binary search
-//      over those indices, the key and the segment's mask -- the record the
-//      attention reads for an index-list selection.
+//   3. one warp sweeps the sorted end points: the union falls into segments
+//      between consecutive end points, each with a constant mask of the
+//      tokens covering it (a token's bit flips at each of its end points: an
+//      exclusive XOR prefix), and a sum prefix over the covered segments
+//      gives each its slot and first union index;
+//   4. every thread writes union positions, four at a time: the segment by a
+//      binary search over those indices, the key and the segment's mask --
+//      the record the attention reads for an index-list selection.
 // At most `cap` positions are written (the union of G tokens' ranges, each
 // covering at most `select` positions, fits).
 __global__ void __launch_bounds__(kRThreads)
@@ -421,41 +422,96 @@ __global__ void __launch_bounds__(kRThreads)
     evs[rank] = a;
   }
   __syncthreads();
-  // 3. the sweep
-  if (threadIdx.x == 0) {
-    uint32_t mask = 0;
-    int nseg = 0;
-    int64_t u = 0;
-    int prev = 0;
-    for (int k = 0; k < ne; ++k) {
-      const int2 e = evs[k];
-      if (e.x == INT32_MAX) break;
-      if (mask != 0 && e.x > prev) {
-        seg_lo[nseg] = prev;
-        seg_mask[nseg] = mask;
-        seg_off[nseg] = u;
-        u += e.x - prev;
-        ++nseg;
-      }
-      mask ^= 1u << e.y;
-      prev = e.x;
+  // 3. the sweep, by warp 0: lane l takes end points [8 l, 8 l + 8)
+  if (threadIdx.x < 32) {
+    constexpr int kPer = kMaxEv / 32;
+    const int lane = threadIdx.x;
+    int x[kPer + 1];
+    uint32_t flip[kPer];
+#pragma unroll
+    for (int j = 0; j <= kPer; ++j) {
+      const int k = kPer * lane + j;
+      const int2 e = k < ne ? evs[k] : make_int2(INT32_MAX, 0);
+      x[j] = e.x;
+      if (j < kPer) flip[j] = e.x == INT32_MAX ? 0u : 1u << e.y;
     }
-    seg_off[nseg] = u;
-    s_nseg = nseg;
+    // the mask after each end point: an exclusive XOR prefix over the lanes
+    uint32_t own = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) own ^= flip[j];
+    uint32_t pre = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, pre, o);
+      if (lane >= o) pre ^= y;
+    }
+    pre ^= own;
+    // covered segments [x_j, x_j+1): their count and length per lane, then
+    // sum prefixes for each one's slot and first union index
+    uint32_t mask[kPer];
+    int cnt = 0;
+    int64_t len = 0;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      pre ^= flip[j];
+      mask[j] = pre;
+      const bool cov = pre != 0u && x[j + 1] != INT32_MAX && x[j + 1] > x[j];
+      cnt += cov;
+      len += cov ? x[j + 1] - x[j] : 0;
+    }
+    int c_in = cnt;
+    int64_t l_in = len;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yc = __shfl_up_sync(0xFFFFFFFFu, c_in, o);
+      const int64_t yl = __shfl_up_sync(0xFFFFFFFFu, l_in, o);
+      if (lane >= o) {
+        c_in += yc;
+        l_in += yl;
+      }
+    }
+    int slot = c_in - cnt;
+    int64_t u = l_in - len;
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      if (mask[j] != 0u && x[j + 1] != INT32_MAX && x[j + 1] > x[j]) {
+        seg_lo[slot] = x[j];
+        seg_mask[slot] = mask[j];
+        seg_off[slot] = u;
+        u += x[j + 1] - x[j];
+        ++slot;
+      }
+    }
+    if (lane == 31) {
+      seg_off[c_in] = l_in;
+      s_nseg = c_in;
+    }
   }
   __syncthreads();
   const int nseg = s_nseg;
   const int64_t U = min(seg_off[nseg], cap);
   if (threadIdx.x == 0) *reinterpret_cast<int32_t*>(rec) = (int32_t)U;
-  // 4. the union positions
-  for (int64_t u = threadIdx.x; u < U; u += kRThreads) {
-    int a = 0, b = nseg - 1;  // the last segment whose first index is <= u
-    while (a < b) {
-      const int c = (a + b + 1) >> 1;
-      if (seg_off[c] <= u) a = c; else b = c - 1;
+  // 4. the union positions, four of a thread at a time
+  for (int64_t u0 = threadIdx.x; u0 < U; u0 += 4 * kRThreads) {
+    int a[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t u = u0 + q * kRThreads;
+      int lo = 0, hi = nseg - 1;  // the last segment whose first index is <= u
+      while (lo < hi) {
+        const int c = (lo + hi + 1) >> 1;
+        if (seg_off[c] <= u) lo = c; else hi = c - 1;
+      }
+      a[q] = lo;
     }
-    keys[u] = seg_lo[a] + (int32_t)(u - seg_off[a]);
-    masks[u] = seg_mask[a];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int64_t u = u0 + q * kRThreads;
+      if (u < U) {
+        keys[u] = seg_lo[a[q]] + (int32_t)(u - seg_off[a[q]]);
+        masks[u] = seg_mask[a[q]];
+      }
+    }
   }
 }
 
