@@ -893,6 +893,8 @@ def main():
                     help="time only the fused producer + selection against the two-step path")
     ap.add_argument("--attention-only", action="store_true",
                     help="time only the grouped masked sparse attention and print its JSON")
+    ap.add_argument("--attention-ranges-only", action="store_true",
+                    help="time only the range form of the grouped attention and print its JSON")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the supplementary decode / single-row / scan-mode timings")
     ap.add_argument("--extra", action="append", choices=sorted(EXTRAS),
@@ -911,6 +913,14 @@ def main():
         dsa.build()
         dsa.load()
         print(json.dumps(measure_attention(dsa, torch, torch.device("cuda:0"))), flush=True)
+        return
+    if args.attention_ranges_only:
+        import torch
+
+        import sparse_attention_indexer_live_gb300 as dsa
+        dsa.build()
+        dsa.load()
+        print(json.dumps(measure_attention_ranges(dsa, torch, torch.device("cuda:0"))), flush=True)
         return
     if args.producer_only or args.fused_only:
         import torch
