@@ -437,19 +437,12 @@ def measure_scan(dsa, torch, dev, local, prefill):
 
 
 def measure_combine(dsa, torch, dev, local, prefill):
-    """Top-k / sliding-window combine on the prefill chunk's top-k."""
+    """Top-k / sliding-window combine on the prefill chunk's top-k (20 launches
+    in one CUDA graph)."""
     wlp, plan_p, logits_p, ends_p, topk_p = prefill
     window = 128
     comb = torch.empty((wlp.rows, wlp.row_topk + window), dtype=torch.int32, device=dev)
-    for _ in range(3):
-        dsa.dsa_combine_window(plan_p, None, ends_p, topk_p, window, comb)
-    e0, e1 = _events(torch, 2)
-    e0.record()
-    for _ in range(20):
-        dsa.dsa_combine_window(plan_p, None, ends_p, topk_p, window, comb)
-    e1.record()
-    torch.cuda.synchronize()
-    us = e0.elapsed_time(e1) * 1e3 / 20
+    us = _graph_timed(torch, lambda: dsa.dsa_combine_window(plan_p, None, ends_p, topk_p, window, comb))
     comb_alg = wlp.rows * (4 * wlp.row_topk + 4 * (wlp.row_topk + window) + 8)
     peak, _ = hbm_peak()
     return {"window": window, "us_per_launch": us, "achieved_gbs": comb_alg / (us * 1e-6) / 1e9,

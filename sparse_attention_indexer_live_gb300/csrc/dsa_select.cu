@@ -1576,22 +1576,38 @@ constexpr int kCombineThreads = 256;
 
 __global__ void __launch_bounds__(kCombineThreads) combine_window_kernel(const Params p, const int32_t* topk,
                                                                          int32_t window, int32_t* out) {
+  extern __shared__ int32_t ts[];  // the row's top-k list, staged once (K entries)
   __shared__ int s_cnt;
   const int r = blockIdx.x;
   const Row R = load_row(p, r);
   const int K = p.K;
-  const int32_t* t = topk + (int64_t)r * K;
+  const int32_t* gt = topk + (int64_t)r * K;
   const int64_t width = (int64_t)K + window;
   int32_t* o = out + (int64_t)r * width;
   const int64_t w1 = R.s + R.L;
   const int64_t w0 = w1 - window > R.s ? w1 - window : R.s;
   const int nw = (int)(w1 - w0);
   if (threadIdx.x == 0) s_cnt = 0;
-  __syncthreads();
+  // the list into shared memory in one pass (16-byte loads when aligned), so
+  // that the searches below do not wait on global memory step by step
   int mine = 0;
-  for (int i = threadIdx.x; i < K; i += kCombineThreads) mine += t[i] >= 0;
+  if ((K & 3) == 0 && (reinterpret_cast<uintptr_t>(gt) & 15) == 0) {
+    for (int i = 4 * threadIdx.x; i < K; i += 4 * kCombineThreads) {
+      const int4 v = __ldg(reinterpret_cast<const int4*>(gt + i));
+      *reinterpret_cast<int4*>(ts + i) = v;
+      mine += (v.x >= 0) + (v.y >= 0) + (v.z >= 0) + (v.w >= 0);
+    }
+  } else {
+    for (int i = threadIdx.x; i < K; i += kCombineThreads) {
+      const int32_t v = __ldg(gt + i);
+      ts[i] = v;
+      mine += v >= 0;
+    }
+  }
+  __syncthreads();
   atomicAdd(&s_cnt, mine);
   __syncthreads();
+  const int32_t* t = ts;
   const int nt = s_cnt;  // valid entries: an ascending prefix of the list
   int lo = 0, hi = nt;
   while (lo < hi) {
@@ -2009,7 +2025,8 @@ int dsa_combine_window(const dsa_select_plan* plan, const int32_t* starts, const
   Params P = plan->base;
   P.starts = starts;
   P.ends = ends;
-  combine_window_kernel<<<plan->cfg.rows, kCombineThreads, 0, (cudaStream_t)stream>>>(P, topk, window, out);
+  combine_window_kernel<<<plan->cfg.rows, kCombineThreads, (size_t)plan->cfg.row_topk * 4, (cudaStream_t)stream>>>(
+      P, topk, window, out);
   return finish_launch(cudaSuccess);
 }
 
