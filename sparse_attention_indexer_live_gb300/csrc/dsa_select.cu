@@ -1536,33 +1536,75 @@ __global__ void __launch_bounds__(kThreads, 2) topk_scan_kernel(const Params p) 
   __syncthreads();
   if (sh.cnt > K) compact_best(buf, keep, K, q.cap, sh);
   const int ng = min(sh.cnt, K);
-  // 2. their ids in ascending order (keep is free again: sort there)
+  // 2. their ids in ascending order, into keep (free again).  Usually as a
+  // bitmap over the row's groups, past the K entries of buf, enumerated in
+  // order; a bitonic sort when the bitmap does not fit there.
   int32_t* ids = reinterpret_cast<int32_t*>(keep);
-  int n2 = 1;
-  while (n2 < ng) n2 <<= 1;
-  for (int i = threadIdx.x; i < n2; i += kThreads) ids[i] = i < ng ? (int32_t)comp_index(buf[i]) : INT32_MAX;
-  __syncthreads();
-  bitonic_sort_i32(ids, n2);
-  // 3. gather the groups' columns in column order (buf is free again)
+  const int64_t bm_words = ((int64_t)G.nb + 31) >> 5;
+  if (bm_words * 4 <= (int64_t)(region_entries - K) * 8) {
+    uint32_t* gbm = reinterpret_cast<uint32_t*>(buf + K);
+    for (int64_t w = threadIdx.x; w < bm_words; w += kThreads) gbm[w] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < ng; i += kThreads) {
+      const uint32_t id = comp_index(buf[i]);
+      atomicOr(&gbm[id >> 5], 1u << (id & 31));
+    }
+    __syncthreads();
+    enumerate_bits(gbm, G.nb, ids, K, sh);  // ends with a barrier
+  } else {
+    int n2 = 1;
+    while (n2 < ng) n2 <<= 1;
+    for (int i = threadIdx.x; i < n2; i += kThreads) ids[i] = i < ng ? (int32_t)comp_index(buf[i]) : INT32_MAX;
+    __syncthreads();
+    bitonic_sort_i32(ids, n2);
+  }
+  // 3. gather the groups' columns in column order (buf is free again), eight
+  // loads of a thread in flight before its stores
   const int64_t ec = s + L;
   const int64_t cs = p.col_stride;
   const int ncand = ng * kScanGroup;
-  for (int t = threadIdx.x; t < ncand; t += kThreads) {
-    const int64_t c = s + (int64_t)ids[t / kScanGroup] * kScanGroup + (t % kScanGroup);
-    buf[t] = c < ec ? compose(order_key(__float_as_uint(__ldcg(rowp + c * cs))), (uint32_t)c) : 0;
+  constexpr int kGatherBatch = 8;
+  for (int t0 = threadIdx.x; t0 < ncand; t0 += kGatherBatch * kThreads) {
+    int64_t cc[kGatherBatch];
+    float v[kGatherBatch];
+#pragma unroll
+    for (int u = 0; u < kGatherBatch; ++u) {
+      const int t = t0 + u * kThreads;
+      cc[u] = t < ncand ? s + (int64_t)ids[t / kScanGroup] * kScanGroup + (t % kScanGroup) : ec;
+      v[u] = cc[u] < ec ? __ldcg(rowp + cc[u] * cs) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < kGatherBatch; ++u) {
+      const int t = t0 + u * kThreads;
+      if (t < ncand) buf[t] = cc[u] < ec ? compose(order_key(__float_as_uint(v[u])), (uint32_t)cc[u]) : 0;
+    }
   }
   __syncthreads();
-  // 4. the K best candidates, emitted in column order
+  // 4. the K best candidates, emitted in column order: each warp takes a
+  // contiguous segment of buf, lane-interleaved (no bank conflicts), counts,
+  // then writes after a prefix over the warps
   const uint64_t X = select_kth(buf, ncand, K, sh);
-  const int per = (ncand + kThreads - 1) / kThreads;
-  const int i0 = threadIdx.x * per;
-  const int i1 = min(i0 + per, ncand);
-  int cnt = 0;
-  for (int i = i0; i < i1; ++i) cnt += buf[i] != 0 && buf[i] >= X;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = (ncand + kWarps - 1) / kWarps;
+  const int a0 = min(warp * seg, ncand), a1 = min(a0 + seg, ncand);
+  int wcnt = 0;
+  for (int i0 = a0; i0 < a1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool f = i < a1 && buf[i] != 0 && buf[i] >= X;
+    wcnt += __popc(__ballot_sync(kFull, f));
+  }
   int total;
-  int pos = block_exclusive_scan(cnt, &total, sh);
-  for (int i = i0; i < i1; ++i)
-    if (buf[i] != 0 && buf[i] >= X && pos < K) out[pos++] = (int32_t)comp_index(buf[i]);
+  int pos = block_exclusive_scan(lane == 0 ? wcnt : 0, &total, sh);
+  pos = __shfl_sync(kFull, pos, 0);
+  const uint32_t lt = lanemask_lt();
+  for (int i0 = a0; i0 < a1; i0 += 32) {
+    const int i = i0 + lane;
+    const bool f = i < a1 && buf[i] != 0 && buf[i] >= X;
+    const uint32_t bal = __ballot_sync(kFull, f);
+    const int o = pos + __popc(bal & lt);
+    if (f && o < K) out[o] = (int32_t)comp_index(buf[i]);
+    pos += __popc(bal);
+  }
 }
 
 // Consumer step: the ascending union of each row's top-k indices and the
