@@ -97,6 +97,7 @@ struct Shared {
   uint32_t sel_count;
   int32_t counts[4];
   int32_t part[kMaxSplit + 1];  // cluster leader: per-CTA counts, then offsets
+  int32_t kept_n;               // finish_block_topk: live kept ids left sorted in `keep`, or -1
   uint64_t tau;
 };
 
@@ -532,10 +533,29 @@ __device__ void finish_block_topk(const Params& p, const Row& R, int r, uint64_t
   }
   __syncthreads();
   int32_t* crow = p.cand + (int64_t)r * (Kb + 1);
-  // the fast path sets only ids below n_b + (take - n); the general one any
-  const int64_t span = fast ? (int64_t)R.nb + (take - n > 0 ? take - n : 0) : p.nblocks;
-  const int got = min(enumerate_bits(bitmap, span, crow, Kb, sh), Kb);
-  for (int i = got + threadIdx.x; i < Kb; i += kThreads) crow[i] = -1;
+  if (fast && n <= kThreads) {
+    // cand without walking the bitmap: the live ids ranked among themselves
+    // (distinct; one thread each), then the padding ids n_b, n_b + 1, ...,
+    // which lie above every live id.  The sorted live ids stay in `keep`
+    // (free after the compaction) for the row top-k.
+    int32_t* sorted = reinterpret_cast<int32_t*>(keep);
+    if (threadIdx.x < n) {
+      const uint32_t id = comp_index(buf[threadIdx.x]);
+      int rank = 0;
+      for (int j = 0; j < n; ++j) rank += comp_index(buf[j]) < id;
+      sorted[rank] = (int32_t)id;
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < Kb; i += kThreads)
+      crow[i] = i < n ? sorted[i] : (i < take ? (int32_t)(R.nb + (i - n)) : -1);
+    if (threadIdx.x == 0) sh.kept_n = n;
+  } else {
+    // the fast path sets only ids below n_b + (take - n); the general one any
+    const int64_t span = fast ? (int64_t)R.nb + (take - n > 0 ? take - n : 0) : p.nblocks;
+    const int got = min(enumerate_bits(bitmap, span, crow, Kb, sh), Kb);
+    for (int i = got + threadIdx.x; i < Kb; i += kThreads) crow[i] = -1;
+    if (threadIdx.x == 0) sh.kept_n = -1;
+  }
   __syncthreads();  // every thread is done reading the bitmap before the pin bit goes in
   if (threadIdx.x == 0) {
     int32_t pin = -1;
@@ -629,9 +649,14 @@ struct RowValues {
 // `src` supplies the values of kept columns: src.prep(kb, nkb) runs once the
 // kept block ids kb[0 .. nkb) (ascending) are known, src.load(j, c) returns
 // column c, a column of block kb[j] (j = -1: the block is not given).
+//
+// `sorted` (may be null): the kept live block ids ascending, n_sorted of them,
+// as finish_block_topk leaves them; the kept list is then those ids with the
+// pin inserted when its bit is set, instead of a walk over the bitmap.
 template <class Src>
 __device__ void row_topk_kept(const Params& p, Src& src, const Row& R, int r, const uint32_t* bitmap,
-                              bool edge, uint8_t* region, Shared& sh) {
+                              bool edge, uint8_t* region, Shared& sh, const int32_t* sorted = nullptr,
+                              int n_sorted = -1) {
   const int K = p.K;
   int32_t* out = p.topk + (int64_t)r * K;
   const int64_t s = R.s;
@@ -650,7 +675,21 @@ __device__ void row_topk_kept(const Params& p, Src& src, const Row& R, int r, co
   const int64_t ec = s + L;
   const int B = p.B;
 
-  const int nkb = min(enumerate_bits(bitmap, R.nb, kb, p.Kb + 1, sh), p.Kb + 1);
+  int nkb;
+  if (sorted && n_sorted >= 0) {
+    // the pin's bit is set only when its block lies inside the buffer (then
+    // below n_b); it joins the list unless a live id already holds it
+    const int64_t pin = R.e > s ? (R.e - 1 - s) / B : -1;
+    const bool pin_set = pin >= 0 && pin < R.nb && bit_set(bitmap, pin);
+    const int pos = pin_set ? lower_bound_i32(sorted, n_sorted, (int32_t)pin) : n_sorted;
+    const bool ins = pin_set && !(pos < n_sorted && sorted[pos] == (int32_t)pin);
+    for (int i = threadIdx.x; i < n_sorted; i += kThreads) kb[i + (ins && i >= pos ? 1 : 0)] = sorted[i];
+    if (ins && threadIdx.x == 0) kb[pos] = (int32_t)pin;
+    nkb = min(n_sorted + (ins ? 1 : 0), p.Kb + 1);
+    __syncthreads();
+  } else {
+    nkb = min(enumerate_bits(bitmap, R.nb, kb, p.Kb + 1, sh), p.Kb + 1);
+  }
   src.prep(kb, nkb);
   // the edge column W-1 is a candidate of its own when its block is not kept
   const bool edge_extra = edge && ec == W && (W - 1) >= s && !bit_set(bitmap, R.nb - 1);
@@ -1326,7 +1365,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   if (kTopK && rank == 0) {
     __syncthreads();
     RowValues src{rowp, p.col_stride};
-    row_topk_kept(p, src, R, r, bitmap, edge, region, sh);
+    row_topk_kept(p, src, R, r, bitmap, edge, region, sh, reinterpret_cast<const int32_t*>(keep), sh.kept_n);
   }
 }
 
