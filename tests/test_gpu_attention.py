@@ -303,6 +303,21 @@ def test_ranges_overlapping_empty_and_clipped():
     _run_ranges(T, H, S, ranges, select=3 * 450, seed=20)
 
 
+def test_ranges_at_the_limits():
+    # 8 ranges a token and 16 tokens a group: 256 end points, the most the
+    # sweep takes; end points shared between tokens (ties in the sort),
+    # ranges touching inside a token (merged), and a ragged last group
+    rng = np.random.default_rng(25)
+    T, H, S = 37, 8, 2000
+    grid = np.arange(0, S + 1, 50)  # shared end points
+    lo = rng.choice(grid[:-1], size=(T, 8))
+    ln = 50 * rng.integers(0, 4, size=(T, 8))
+    ranges = np.stack([lo, lo + ln], axis=2).astype(np.int32)
+    ranges[3, :, 0] = np.arange(8) * 100  # touching pairs inside one token
+    ranges[3, :, 1] = np.arange(8) * 100 + 100
+    _run_ranges(T, H, S, ranges, select=8 * 150 + 800, seed=26)
+
+
 def test_ranges_graph_replay_follows_new_ranges():
     # the range form captured once replays on new ranges written into the
     # captured buffer, and gives what a direct call gives
