@@ -77,7 +77,13 @@ typedef struct dsa_select_cfg {
   int32_t split;         /* CTAs per row in the select kernels: 0 = automatic (from
                             rows, W and the SM count), else a power of two <= 16
                             (a thread-block cluster per row when > 1); reduced when
-                            the device cannot schedule it                           */
+                            the device cannot schedule it.  32 .. 256 (a power of
+                            two): a wide split -- each row is first streamed in
+                            `split` parts, each keeping its top-Kb list in device
+                            memory the plan owns, and a 16-CTA cluster per row then
+                            merges them.  Automatic for very few rows of many
+                            blocks (rows * 64 <= SMs).  A plan with a wide split
+                            must not run two calls at once (the lists are shared).  */
 } dsa_select_cfg;
 
 typedef struct dsa_select_plan dsa_select_plan;
@@ -97,7 +103,7 @@ typedef struct dsa_plan_desc {
   int32_t ctas_per_sm_select;/* resident select CTAs per SM (unclustered kernel)        */
   int32_t grid_select;       /* CTAs per select launch (rows * split)                  */
   int32_t split;             /* CTAs per row chosen by the plan                        */
-  int32_t reserved;
+  int32_t parts;             /* wide split: parts per row of the first launch (0: none) */
 } dsa_plan_desc;
 
 /*

@@ -32,7 +32,7 @@ class dsa_plan_desc(ctypes.Structure):
                 ("candidate_capacity", ctypes.c_int32), ("smem_select", ctypes.c_int64),
                 ("smem_topk_cand", ctypes.c_int64), ("smem_topk_scan", ctypes.c_int64),
                 ("ctas_per_sm_select", ctypes.c_int32), ("grid_select", ctypes.c_int32),
-                ("split", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("split", ctypes.c_int32), ("parts", ctypes.c_int32)]
 
 
 EXPORTS = ("dsa_select_init", "dsa_select_destroy", "dsa_plan_describe", "dsa_candidate_select",

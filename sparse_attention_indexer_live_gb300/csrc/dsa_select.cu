@@ -50,6 +50,8 @@ constexpr int kMaxTopK = 4096;
 constexpr int kMaxBlockTopK = 4096;
 constexpr int kMaxBlockSize = 4096;
 constexpr int kMaxSplit = 16;                 // CTAs per row (thread-block cluster size)
+constexpr int kMaxParts = 256;                // wide split: parts per row of its first launch
+constexpr int kWideParts = 64;                // ... chosen automatically for very few long rows
 constexpr int32_t kMinBlocksPerCta = 1024;    // smallest share of a row's blocks worth a CTA
 
 namespace cg = cooperative_groups;
@@ -83,6 +85,8 @@ struct Params {
   int32_t epoch;         // streaming rounds between two capacity checks (128-bit path)
   int32_t scan_epoch;    // the same for the scan-mode buffer
   int32_t small_cap;     // candidate entries of the short-row path (0: path off)
+  uint64_t* parts_ws;    // wide split: per-part top-Kb lists (nullptr: the cluster streams itself)
+  int32_t nparts;        // wide split: parts per row in the first launch
 };
 
 // Scratch with a fixed size, in static shared memory.
@@ -1284,6 +1288,7 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   if constexpr (kCluster) {
     const int64_t want = ((int64_t)R.nb + kMinBlocksPerCta - 1) / kMinBlocksPerCta;
     parts = (int)(want < k ? (want > 0 ? want : 1) : k);
+    if (p.parts_ws) parts = k;  // wide split: every CTA of the cluster takes part
     if (parts == 1 && rank != 0) return;
     if (rank < parts) {
       j0 = (int32_t)((int64_t)R.nb * rank / parts);
@@ -1307,7 +1312,27 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   __syncthreads();
   const bool clustered = kCluster && parts > 1;
   const int kk = clustered ? k : 1;
-  stream_block_maxima(p, rowp, R, j0, j1, buf, keep, sh);
+  if (kCluster && p.parts_ws) {
+    // wide split: the first launch streamed the row in p.nparts parts, each
+    // leaving its top-Kb list; this CTA takes lists rank, rank + k, ... (the
+    // top-Kb of their union is the top-Kb of their blocks).  This launch is a
+    // programmatic dependent of that one: wait for it before the first read.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (threadIdx.x == 0) {
+      int c = 0;
+      for (int l = rank; l < p.nparts; l += k) c += (int)p.parts_ws[((int64_t)r * p.nparts + l) * (p.Kb + 1)];
+      sh.cnt = c;
+    }
+    int off = 0;
+    for (int l = rank; l < p.nparts; l += k) {
+      const uint64_t* lst = p.parts_ws + ((int64_t)r * p.nparts + l) * (p.Kb + 1);
+      const int n = (int)lst[0];
+      for (int i = threadIdx.x; i < n; i += kThreads) buf[off + i] = lst[1 + i];
+      off += n;
+    }
+  } else {
+    stream_block_maxima(p, rowp, R, j0, j1, buf, keep, sh);
+  }
   __syncthreads();
 
   if (clustered) {
@@ -1367,6 +1392,39 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
     RowValues src{rowp, p.col_stride};
     row_topk_kept(p, src, R, r, bitmap, edge, region, sh, reinterpret_cast<const int32_t*>(keep), sh.kept_n);
   }
+}
+
+// Wide split, first launch: part `q` of row r streams its share of the live
+// blocks [nb q / P, nb (q + 1) / P) exactly as a cluster CTA streams its
+// share, keeps its top-Kb and stores it as a list in the plan's workspace:
+// count, then the entries (composites).  The cluster launch that follows
+// loads these lists in place of streaming the row itself.
+__global__ void __launch_bounds__(kThreads, 2) wide_part_kernel(const Params p) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ Shared sh;
+  // the cluster launch that merges these lists may start its own setup now
+  // (it waits for this grid to finish before reading them)
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int P = p.nparts;
+  const int r = blockIdx.x / P, q = blockIdx.x % P;
+  uint64_t* keep = reinterpret_cast<uint64_t*>(dyn + (((size_t)p.bitmap_words * 4 + 15) & ~(size_t)15));
+  uint64_t* buf = keep + p.Kb;
+  const Row R = load_row(p, r);
+  const float* rowp = p.logits + (int64_t)r * p.row_stride;
+  const int32_t j0 = (int32_t)((int64_t)R.nb * q / P);
+  const int32_t j1 = (int32_t)((int64_t)R.nb * (q + 1) / P);
+  if (threadIdx.x == 0) {
+    sh.cnt = 0;
+    sh.tau = 0;
+  }
+  __syncthreads();
+  stream_block_maxima(p, rowp, R, j0, j1, buf, keep, sh);
+  __syncthreads();
+  if (sh.cnt > p.Kb) compact_best(buf, keep, p.Kb, p.cap, sh);
+  const int n = min(sh.cnt, p.Kb);
+  uint64_t* out = p.parts_ws + ((int64_t)r * P + q) * (p.Kb + 1);
+  if (threadIdx.x == 0) out[0] = (uint64_t)n;
+  for (int i = threadIdx.x; i < n; i += kThreads) out[1 + i] = buf[i];
 }
 
 // Fused indexer selection, second launch: the block top-k of one query from
@@ -1733,6 +1791,8 @@ struct dsa_select_plan {
   size_t smem_topk_scan;
   int fused_ok;  // 1 when the plan can take the fused indexer selection
   int ctas_per_sm_select;
+  int nparts;            // wide split: parts per row of the first launch (0: none)
+  uint64_t* parts_ws;    // ... and their lists, device memory owned by the plan
 };
 
 namespace {
@@ -1760,7 +1820,7 @@ int validate(const dsa_select_cfg* c) {
   if (c->rows > 1 && c->row_stride < row_span) return DSA_ERR_INVALID_ARG;
   if (c->row_stride < 0) return DSA_ERR_INVALID_ARG;
   if (c->block_size > kMaxBlockSize || c->block_topk > kMaxBlockTopK || c->row_topk > kMaxTopK ||
-      c->split > kMaxSplit)
+      c->split > kMaxParts)
     return DSA_ERR_UNSUPPORTED;
   return DSA_OK;
 }
@@ -1821,24 +1881,37 @@ Sizes sizes_for(Params& P, int split) {
 }
 
 template <bool kTopK>
-cudaError_t launch_select(const dsa_select_plan* plan, const Params& P, cudaStream_t stream) {
+cudaError_t launch_select(const dsa_select_plan* plan, const Params& P0, cudaStream_t stream) {
   const int k = plan->split;
   if (k <= 1) {
-    select_kernel<kTopK, false><<<plan->cfg.rows, kThreads, plan->smem_select, stream>>>(P);
+    select_kernel<kTopK, false><<<plan->cfg.rows, kThreads, plan->smem_select, stream>>>(P0);
     return cudaSuccess;
+  }
+  Params P = P0;
+  if (plan->nparts > 0) {
+    // wide split: the row's parts first, then the cluster that merges them
+    P.parts_ws = plan->parts_ws;
+    P.nparts = plan->nparts;
+    wide_part_kernel<<<plan->cfg.rows * plan->nparts, kThreads, plan->smem_select, stream>>>(P);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)plan->cfg.rows * (unsigned)k, 1, 1);
   lc.blockDim = dim3(kThreads, 1, 1);
   lc.dynamicSmemBytes = plan->smem_select;
   lc.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)k;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // wide split: a programmatic dependent launch of the parts' launch, so the
+  // clusters are placed and set up while the parts finish
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = plan->nparts > 0 ? 2 : 1;
   return cudaLaunchKernelEx(&lc, select_kernel<kTopK, true>, P);
 }
 
@@ -1930,6 +2003,8 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
   int rc = DSA_OK;
   int ctas = 0;
   int split = 1;
+  int nparts = 0;
+  uint64_t* parts_ws = nullptr;
   Sizes z = sizes_for(P, 1);
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
       cudaDeviceGetAttribute(&smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
@@ -1941,11 +2016,20 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
     // -- a decode batch -- runs one CTA per row: its rows are short, and the
     // cluster launch would cost more than it saves.)
     int want = cfg->split;
+    if (want > kMaxSplit) {  // a wide split: `want` parts, then a cluster per row
+      nparts = want;
+      want = kMaxSplit;
+    }
     if (want == 0) {
       want = 1;
       while (want < kMaxSplit && (int64_t)cfg->rows * want * 2 <= (int64_t)sms &&
              P.nblocks >= (int64_t)2 * want * kMinBlocksPerCta)
         want *= 2;
+      // very few long rows leave most SMs idle even with a cluster per row:
+      // stream each row in kWideParts parts first
+      if (want == kMaxSplit && (int64_t)cfg->rows * kMaxSplit * 4 <= (int64_t)sms &&
+          P.nblocks >= (int64_t)kWideParts * kMinBlocksPerCta)
+        nparts = kWideParts;
     }
     for (split = want; split >= 1; split /= 2) {
       z = sizes_for(P, split);
@@ -1969,6 +2053,19 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
       rc = DSA_ERR_CUDA;
     }
   }
+  // the wide split needs a cluster per row, and each cluster CTA's lists must
+  // fit its streaming buffer
+  if (split <= 1 || ((int64_t)(nparts + split - 1) / split) * cfg->block_topk > z.cap) nparts = 0;
+  if (rc == DSA_OK && nparts > 0) {
+    const size_t bytes = (size_t)cfg->rows * nparts * (cfg->block_topk + 1) * 8;
+    if (cudaFuncSetAttribute(wide_part_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)z.select) !=
+            cudaSuccess ||
+        (bytes > 0 && cudaMalloc(&parts_ws, bytes) != cudaSuccess)) {
+      cudaGetLastError();
+      parts_ws = nullptr;
+      nparts = 0;  // the plan still serves every call, with a cluster per row
+    }
+  }
   int fused_ok = rc == DSA_OK && fusable(cfg);
   if (fused_ok && (cudaFuncSetAttribute(fused_blocks_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         (int)z.select) != cudaSuccess ||
@@ -1983,7 +2080,10 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
     return rc;
   }
   dsa_select_plan* pl = new (std::nothrow) dsa_select_plan;
-  if (!pl) return DSA_ERR_UNSUPPORTED;
+  if (!pl) {
+    if (parts_ws) cudaFree(parts_ws);
+    return DSA_ERR_UNSUPPORTED;
+  }
   pl->cfg = *cfg;
   pl->device = device;
   pl->sm_count = sms;
@@ -1998,12 +2098,25 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
   pl->smem_topk_scan = z.scan;
   pl->fused_ok = fused_ok;
   pl->ctas_per_sm_select = ctas;
+  pl->nparts = nparts;
+  pl->parts_ws = parts_ws;
   *plan = pl;
   if (workspace_bytes) *workspace_bytes = 0;
   return DSA_OK;
 }
 
-void dsa_select_destroy(dsa_select_plan* plan) { delete plan; }
+void dsa_select_destroy(dsa_select_plan* plan) {
+  if (!plan) return;
+  if (plan->parts_ws) {
+    int prev = -1;
+    cudaGetDevice(&prev);
+    cudaSetDevice(plan->device);
+    cudaFree(plan->parts_ws);
+    if (prev >= 0 && prev != plan->device) cudaSetDevice(prev);
+    cudaGetLastError();
+  }
+  delete plan;
+}
 
 int dsa_plan_describe(const dsa_select_plan* plan, dsa_plan_desc* out) {
   if (!plan || !out) return DSA_ERR_INVALID_ARG;
@@ -2021,6 +2134,7 @@ int dsa_plan_describe(const dsa_select_plan* plan, dsa_plan_desc* out) {
   out->ctas_per_sm_select = plan->ctas_per_sm_select;
   out->grid_select = plan->cfg.rows * plan->split;
   out->split = plan->split;
+  out->parts = plan->nparts;
   return DSA_OK;
 }
 

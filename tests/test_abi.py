@@ -73,7 +73,7 @@ def test_invalid_shapes_rejected_before_cuda(lib, kw):
 
 
 @pytest.mark.parametrize("kw", [dict(row_topk=4097), dict(block_topk=5000),
-                                dict(block_size=5000), dict(split=32)])
+                                dict(block_size=5000), dict(split=512)])
 def test_out_of_range_shapes_unsupported(lib, kw):
     assert _init(lib, **kw) == dsa.DSA_ERR_UNSUPPORTED
 

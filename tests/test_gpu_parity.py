@@ -110,11 +110,13 @@ def test_ascending_values_force_many_compactions():
     check_all_modes(case, what="monotone")
 
 
-@pytest.mark.parametrize("split", [2, 4, 16])
+@pytest.mark.parametrize("split", [2, 4, 16, 32, 64])
 @pytest.mark.parametrize("layout", ["aligned", "misaligned", "stride2", "b1"])
 def test_cluster_split_rows(split, layout):
     """k CTAs per row in a thread-block cluster: each streams a share of the
-    blocks, the leader merges the shares over distributed shared memory."""
+    blocks, the leader merges the shares over distributed shared memory.
+    split 32 / 64: the wide split -- the row streamed in that many parts by a
+    first launch, their top-Kb lists merged by a 16-CTA cluster."""
     rng = np.random.default_rng(split * 13 + len(layout))
     W, B, cs, starts = 200_000, 8, 1, [0, 4, 0, 100]
     if layout == "misaligned":
@@ -129,7 +131,11 @@ def test_cluster_split_rows(split, layout):
     case = Case(x, starts, ends, width=W, block_size=B, block_topk=256, row_topk=2048,
                 col_stride=cs, row_stride=W * cs, split=split)
     run = DeviceRun(case)
-    assert run.plan.describe()["split"] == split
+    desc = run.plan.describe()
+    if split <= 16:
+        assert desc["split"] == split and desc["parts"] == 0
+    else:
+        assert desc["split"] == 16 and desc["parts"] == split
     check_all_modes(case, what=f"split={split} {layout}")
 
 
@@ -143,8 +149,9 @@ def test_cluster_split_edge_rows():
     starts = [W + 5, 0, 0, 0, 17, 0, 3, 0]
     ends = [W + 20, 0, -4, W, W + 9, 1, 65_000, W + 16]
     for Kb, K in ((256, 2048), (3, 40), (1, 4096)):
-        case = Case(x, starts, ends, width=W, block_size=8, block_topk=Kb, row_topk=K, split=8)
-        check_all_modes(case, what=f"cluster edges Kb={Kb} K={K}")
+        for split in (8, 32):
+            case = Case(x, starts, ends, width=W, block_size=8, block_topk=Kb, row_topk=K, split=split)
+            check_all_modes(case, what=f"cluster edges Kb={Kb} K={K} split={split}")
 
 
 def test_auto_split_for_few_long_rows():
@@ -153,7 +160,11 @@ def test_auto_split_for_few_long_rows():
     many = dsa.dsa_select_init(rows=2048, width=1 << 20, block_size=8, block_topk=256,
                                row_topk=2048)
     assert few.describe()["split"] >= 8
-    assert many.describe()["split"] == 1
+    assert many.describe()["split"] == 1 and many.describe()["parts"] == 0
+    # one 1M-column row leaves most SMs idle even with a 16-CTA cluster: the
+    # wide split streams it in 64 parts first
+    if few.describe()["sm_count"] >= 64 and few.describe()["split"] == 16:
+        assert few.describe()["parts"] == 64
 
 
 def test_tiny_workload_full():
