@@ -112,7 +112,11 @@ typedef struct dsa_plan_desc {
  * reads the device's SM count and shared-memory limit and configures the
  * kernels.  *plan receives a host object freed by dsa_select_destroy;
  * *workspace_bytes (may be NULL) receives the device workspace every call of
- * this plan needs (0 for this build: pass NULL).
+ * this plan needs (0 for this build: pass NULL).  A plan with a wide split
+ * (see dsa_select_cfg.split) allocates its own device memory for the parts'
+ * lists here, rows * parts * (Kb + 1) * 8 bytes, and frees it in
+ * dsa_select_destroy; if that allocation fails the plan keeps a cluster per
+ * row instead.
  */
 int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** plan,
                     size_t* workspace_bytes);
