@@ -167,6 +167,27 @@ def test_auto_split_for_few_long_rows():
         assert few.describe()["parts"] == 64
 
 
+@pytest.mark.parametrize("rows", [1, 2])
+def test_one_or_two_1m_rows_auto_plan(rows):
+    """P1's test plan: a single row over a 1M-column buffer -- in the plan the
+    device picks for it (on GB300 the wide split: 64 parts, then a 16-CTA
+    cluster per row), every column and index compared with the oracle in all
+    three modes.  The second row has a start, an end short of W and a spike
+    mix; a third shape puts the pin past W."""
+    W = 1 << 20
+    rng = np.random.default_rng(90 + rows)
+    x = rng.standard_normal((rows, W)).astype(np.float32)
+    x[:, rng.integers(0, W, 64)] = 6.0 + np.abs(rng.standard_normal(64)).astype(np.float32)
+    if rows == 1:
+        cases = [(None, [W]), (None, [W + 5])]  # full width; pin past W (edge column)
+    else:
+        x[1, 300_000:300_800] = -np.inf
+        cases = [([0, 17], [W, 900_001]), ([3, 0], [W + 9, W])]
+    for starts, ends in cases:
+        case = Case(x, starts, ends, width=W, block_size=8, block_topk=256, row_topk=2048)
+        check_all_modes(case, what=f"{rows} x 1M rows, starts {starts}, ends {ends}")
+
+
 def test_tiny_workload_full():
     wl = wk.WORKLOADS["tiny"]
     x, s, e = wk.make_all(wl)
