@@ -82,7 +82,8 @@ typedef struct dsa_select_cfg {
                             `split` parts, each keeping its top-Kb list in device
                             memory the plan owns, and a 16-CTA cluster per row then
                             merges them.  Automatic for very few rows of many
-                            blocks (rows * 64 <= SMs).  A plan with a wide split
+                            blocks: 64 parts when rows * 64 <= SMs, 128 when
+                            rows * 128 <= SMs.  A plan with a wide split
                             must not run two calls at once (the lists are shared).  */
 } dsa_select_cfg;
 

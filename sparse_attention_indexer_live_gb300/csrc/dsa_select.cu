@@ -52,6 +52,7 @@ constexpr int kMaxBlockSize = 4096;
 constexpr int kMaxSplit = 16;                 // CTAs per row (thread-block cluster size)
 constexpr int kMaxParts = 256;                // wide split: parts per row of its first launch
 constexpr int kWideParts = 64;                // ... chosen automatically for very few long rows
+                                              // (twice as many where rows * 128 <= SMs)
 constexpr int32_t kMinBlocksPerCta = 1024;    // smallest share of a row's blocks worth a CTA
 
 namespace cg = cooperative_groups;
@@ -273,15 +274,46 @@ __device__ uint64_t select_kth(const uint64_t* a, int n, int k, Shared& sh) {
 
 // Keep the best k of the n = *cnt entries of buf; afterwards *cnt = k and
 // *tau = the k-th best (new entries must beat it).  `keep` holds k entries.
+// kScan: the entries >= the threshold go to keep by a block prefix over the
+// threads' counts (kU entries a thread loaded at once: fewer dependent steps
+// for a CTA's last compactions); else by warp-aggregated appends (no
+// barrier: the compactions inside the streaming loop).
+template <bool kScan = false>
 __device__ void compact_best(uint64_t* buf, uint64_t* keep, int k, int cap, Shared& sh) {
   const int n = min(sh.cnt, cap);
   const uint64_t X = select_kth(buf, n, k, sh);
-  if (threadIdx.x == 0) sh.keep_cnt = 0;
-  __syncthreads();
-  for (int i0 = 0; i0 < n; i0 += kThreads) {
-    const int i = i0 + threadIdx.x;
-    const uint64_t c = i < n ? buf[i] : 0;
-    warp_append(i < n && c >= X, c, keep, &sh.keep_cnt, k);
+  if constexpr (kScan) {
+    constexpr int kU = 4;
+    int done = 0;
+    for (int i0 = 0; i0 < n; i0 += kThreads * kU) {
+      uint64_t v[kU];
+      int cnt = 0;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kThreads + (int)threadIdx.x;
+        v[u] = i < n ? buf[i] : 0;
+        cnt += i < n && v[u] >= X;
+      }
+      int total;
+      int pos = done + block_exclusive_scan(cnt, &total, sh);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kThreads + (int)threadIdx.x;
+        if (i < n && v[u] >= X) {
+          if (pos < k) keep[pos] = v[u];
+          ++pos;
+        }
+      }
+      done += total;
+    }
+  } else {
+    if (threadIdx.x == 0) sh.keep_cnt = 0;
+    __syncthreads();
+    for (int i0 = 0; i0 < n; i0 += kThreads) {
+      const int i = i0 + threadIdx.x;
+      const uint64_t c = i < n ? buf[i] : 0;
+      warp_append(i < n && c >= X, c, keep, &sh.keep_cnt, k);
+    }
   }
   __syncthreads();
   for (int i = threadIdx.x; i < k; i += kThreads) buf[i] = keep[i];
@@ -490,11 +522,14 @@ __device__ void stream_block_maxima(const Params& p, const float* rowp, const Ro
 // Step 2 tail + 3: final block top-k (with the -inf padding blocks past the
 // span), the bitmap of chosen blocks, cand output, the pin and the edge flag.
 // On return the bitmap also holds the pin's block when its packed column is
-// inside the buffer, and sh.edge is set.
+// inside the buffer, and sh.edge is set.  lanes_per_id: rank the kept ids
+// with two or four lanes each (a cluster leader, on whose finish the whole
+// row waits); else one thread an id.
 __device__ void finish_block_topk(const Params& p, const Row& R, int r, uint64_t* buf, uint64_t* keep,
-                                  uint32_t* bitmap, Shared& sh) {
+                                  uint32_t* bitmap, Shared& sh,
+                                  bool lanes_per_id = false) {
   const int Kb = p.Kb;
-  if (sh.cnt > Kb) compact_best(buf, keep, Kb, p.cap, sh);
+  if (sh.cnt > Kb) compact_best<true>(buf, keep, Kb, p.cap, sh);
   // buf now holds the live top-min(Kb, n_b), unordered
   int n = min(sh.cnt, p.cap - Kb);
   const int take = (int)(p.nblocks < Kb ? p.nblocks : Kb);
@@ -543,7 +578,31 @@ __device__ void finish_block_topk(const Params& p, const Row& R, int r, uint64_t
     // which lie above every live id.  The sorted live ids stay in `keep`
     // (free after the compaction) for the row top-k.
     int32_t* sorted = reinterpret_cast<int32_t*>(keep);
-    if (threadIdx.x < n) {
+    if (lanes_per_id && n <= kThreads / 2) {
+      // the ids as an int32 array past the entries (16-byte aligned, padded
+      // to a multiple of 16 with ids above every live one), read four at a
+      // time; g = 2 or 4 neighbouring lanes an id, each counting a share
+      const int n16 = (n + 15) & ~15;
+      int32_t* ids = reinterpret_cast<int32_t*>(((uintptr_t)(buf + n) + 15) & ~(uintptr_t)15);
+      for (int i = threadIdx.x; i < n16; i += kThreads) ids[i] = i < n ? (int32_t)comp_index(buf[i]) : INT32_MAX;
+      __syncthreads();
+      const int lg = n <= kThreads / 4 ? 2 : 1, g = 1 << lg;
+      const int e = threadIdx.x >> lg, sub = threadIdx.x & (g - 1);
+      int32_t id = 0;
+      int rank = 0;
+      if (e < n) {
+        id = ids[e];
+        const int4* v4 = reinterpret_cast<const int4*>(ids);
+#pragma unroll 4
+        for (int j = sub; j < (n16 >> 2); j += g) {
+          const int4 w = v4[j];
+          rank += (w.x < id) + (w.y < id) + (w.z < id) + (w.w < id);
+        }
+      }
+      rank += __shfl_xor_sync(kFull, rank, 1);
+      if (g == 4) rank += __shfl_xor_sync(kFull, rank, 2);
+      if (e < n && sub == 0) sorted[rank] = id;
+    } else if (threadIdx.x < n) {
       const uint32_t id = comp_index(buf[threadIdx.x]);
       int rank = 0;
       for (int j = 0; j < n; ++j) rank += comp_index(buf[j]) < id;
@@ -1318,17 +1377,58 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
     // top-Kb of their union is the top-Kb of their blocks).  This launch is a
     // programmatic dependent of that one: wait for it before the first read.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (threadIdx.x == 0) {
-      int c = 0;
-      for (int l = rank; l < p.nparts; l += k) c += (int)p.parts_ws[((int64_t)r * p.nparts + l) * (p.Kb + 1)];
-      sh.cnt = c;
+    // The counts (one warp) and the entries (every thread) are loaded at
+    // once; a slot past its list's count is loaded but not kept.  sh.hist
+    // holds the counts, then from entry 128 the offsets (at most 128 lists a
+    // CTA: k >= 2, nparts <= 256).
+    const int Kb = p.Kb;
+    const int nl = (p.nparts - rank + k - 1) / k;
+    const int64_t lstride = (int64_t)k * (Kb + 1);
+    const uint64_t* lists = p.parts_ws + ((int64_t)r * p.nparts + rank) * (Kb + 1);
+    const int slots = nl * Kb;
+    constexpr int kPre = 4;
+    uint64_t v[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int t = threadIdx.x + u * kThreads;
+      v[u] = t < slots ? __ldcg(lists + (t / Kb) * lstride + 1 + t % Kb) : 0;
     }
-    int off = 0;
-    for (int l = rank; l < p.nparts; l += k) {
-      const uint64_t* lst = p.parts_ws + ((int64_t)r * p.nparts + l) * (p.Kb + 1);
-      const int n = (int)lst[0];
-      for (int i = threadIdx.x; i < n; i += kThreads) buf[off + i] = lst[1 + i];
-      off += n;
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      uint32_t c[4], tot = 0;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int li = 4 * lane + b;
+        c[b] = li < nl ? (uint32_t)__ldcg(lists + li * lstride) : 0u;
+        tot += c[b];
+      }
+      uint32_t incl = tot;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, d);
+        if (lane >= d) incl += y;
+      }
+      uint32_t off = incl - tot;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        sh.hist[4 * lane + b] = c[b];
+        sh.hist[128 + 4 * lane + b] = off;
+        off += c[b];
+      }
+      if (lane == 31) sh.cnt = (int32_t)incl;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int t = threadIdx.x + u * kThreads;
+      if (t < slots) {
+        const int li = t / Kb, i = t % Kb;
+        if ((uint32_t)i < sh.hist[li]) buf[sh.hist[128 + li] + i] = v[u];
+      }
+    }
+    for (int t = threadIdx.x + kPre * kThreads; t < slots; t += kThreads) {
+      const int li = t / Kb, i = t % Kb;
+      if ((uint32_t)i < sh.hist[li]) buf[sh.hist[128 + li] + i] = __ldcg(lists + li * lstride + 1 + i);
     }
   } else {
     stream_block_maxima(p, rowp, R, j0, j1, buf, keep, sh);
@@ -1337,41 +1437,42 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
 
   if (clustered) {
     cg::cluster_group cl = cg::this_cluster();
-    if (sh.cnt > p.Kb) compact_best(buf, keep, p.Kb, p.cap, sh);  // local top-Kb
+    if (sh.cnt > p.Kb) compact_best<true>(buf, keep, p.Kb, p.cap, sh);  // local top-Kb
     cl.sync();  // every CTA's list is final
+    // every CTA reads the counts; each peer then stores its list into the
+    // leader's buffer at its offset (the leader's own list is at offset 0)
+    if (threadIdx.x < 32) {
+      const int q = threadIdx.x;
+      int c = 0;
+      if (q < k) c = q == rank ? min(sh.cnt, p.Kb) : min(cl.map_shared_rank(&sh, (unsigned)q)->cnt, p.Kb);
+      int incl = c;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (q >= d) incl += y;
+      }
+      if (q == rank) sh.part[0] = incl - c;
+      if (q == k - 1) sh.part[1] = incl;
+    }
+    __syncthreads();
+    if (rank != 0) {
+      uint64_t* dst = cl.map_shared_rank(buf, 0u) + sh.part[0];
+      const int n = min(sh.cnt, p.Kb);
+      for (int i = threadIdx.x; i < n; i += kThreads) dst[i] = buf[i];
+    }
+    cl.sync();  // the leader holds every list
     if (rank == 0) {
-      // every peer's count at once, then all peers' entries in one pass
-      if (threadIdx.x < k) {
-        const int q = threadIdx.x;
-        sh.part[q] = q == 0 ? sh.cnt : min(cl.map_shared_rank(&sh, (unsigned)q)->cnt, p.Kb);
-      }
+      if (threadIdx.x == 0) sh.cnt = sh.part[1];
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int off = 0;
-        for (int q = 0; q < k; ++q) {
-          const int c = sh.part[q];
-          sh.part[q] = off;  // exclusive offset
-          off += c;
-        }
-        sh.part[k] = off;
-      }
-      __syncthreads();
-      const int own = sh.part[1];
-      const int total = sh.part[k];
-      for (int i = own + threadIdx.x; i < total; i += kThreads) {
-        int q = 1;
-        while (q + 1 < k && sh.part[q + 1] <= i) ++q;
-        buf[i] = cl.map_shared_rank(buf, (unsigned)q)[i - sh.part[q]];
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) sh.cnt = total;
-      __syncthreads();
-      finish_block_topk(p, R, r, buf, keep, bitmap, sh);
+      finish_block_topk(p, R, r, buf, keep, bitmap, sh, true);
     }
     cl.sync();  // the leader's bitmap, edge flag and cand are final
     if (rank != 0) {
+      // the bitmap words of this CTA's mask share (below)
+      const int mkc = kTopK ? k - 1 : k, mrc = kTopK ? rank - 1 : rank;
+      const int32_t m0 = (int32_t)((int64_t)R.nb * mrc / mkc), m1 = (int32_t)((int64_t)R.nb * (mrc + 1) / mkc);
       const uint32_t* lbm = cl.map_shared_rank(bitmap, 0u);
-      for (int w = (j0 >> 5) + threadIdx.x; w < ((j1 + 31) >> 5); w += kThreads) bitmap[w] = lbm[w];
+      for (int w = (m0 >> 5) + threadIdx.x; w < ((m1 + 31) >> 5); w += kThreads) bitmap[w] = lbm[w];
       if (threadIdx.x == 0) sh.edge = cl.map_shared_rank(&sh, 0u)->edge;
       __syncthreads();
     }
@@ -1379,19 +1480,28 @@ __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
     finish_block_topk(p, R, r, buf, keep, bitmap, sh);
   }
   const bool edge = sh.edge != 0;
-  // mask: an even share of [0, min(s, ecm)) (column 0 .. start) and our blocks
-  const int64_t P = R.s < (int64_t)R.ecm ? R.s : (int64_t)R.ecm;
-  const int64_t plo = (P * rank / kk) & ~(int64_t)3;
-  const int64_t phi = rank + 1 == kk ? P : ((P * (rank + 1) / kk) & ~(int64_t)3);
-  write_mask(p, rowp, R, bitmap, edge, plo, phi);
-  const int64_t lhi = R.s + (int64_t)j1 * p.B;
-  write_mask(p, rowp, R, bitmap, edge, R.s + (int64_t)j0 * p.B, lhi < R.ecm ? lhi : (int64_t)R.ecm);
-  if (clustered) cg::this_cluster().sync();  // masks visible to the leader
+  // mask: share mr of mk of [0, min(s, ecm)) (column 0 .. start) and of the
+  // live blocks.  In a cluster that also takes the row top-k the leader masks
+  // nothing: it selects meanwhile (the row top-k reads kept columns only,
+  // which the mask never writes) and the other CTAs mask the row.
+  const bool leader_selects = kTopK && clustered;
+  const int mk = leader_selects ? kk - 1 : kk, mr = leader_selects ? rank - 1 : rank;
+  if (mr >= 0) {
+    const int64_t P = R.s < (int64_t)R.ecm ? R.s : (int64_t)R.ecm;
+    const int64_t plo = (P * mr / mk) & ~(int64_t)3;
+    const int64_t phi = mr + 1 == mk ? P : ((P * (mr + 1) / mk) & ~(int64_t)3);
+    write_mask(p, rowp, R, bitmap, edge, plo, phi);
+    const int32_t m0 = (int32_t)((int64_t)R.nb * mr / mk), m1 = (int32_t)((int64_t)R.nb * (mr + 1) / mk);
+    const int64_t lhi = R.s + (int64_t)m1 * p.B;
+    write_mask(p, rowp, R, bitmap, edge, R.s + (int64_t)m0 * p.B, lhi < R.ecm ? lhi : (int64_t)R.ecm);
+  }
   if (kTopK && rank == 0) {
     __syncthreads();
     RowValues src{rowp, p.col_stride};
     row_topk_kept(p, src, R, r, bitmap, edge, region, sh, reinterpret_cast<const int32_t*>(keep), sh.kept_n);
   }
+  // the leader's shared memory stays until every peer has read it
+  if (clustered) cg::this_cluster().sync();
 }
 
 // Wide split, first launch: part `q` of row r streams its share of the live
@@ -1420,7 +1530,7 @@ __global__ void __launch_bounds__(kThreads, 2) wide_part_kernel(const Params p) 
   __syncthreads();
   stream_block_maxima(p, rowp, R, j0, j1, buf, keep, sh);
   __syncthreads();
-  if (sh.cnt > p.Kb) compact_best(buf, keep, p.Kb, p.cap, sh);
+  if (sh.cnt > p.Kb) compact_best<true>(buf, keep, p.Kb, p.cap, sh);
   const int n = min(sh.cnt, p.Kb);
   uint64_t* out = p.parts_ws + ((int64_t)r * P + q) * (p.Kb + 1);
   if (threadIdx.x == 0) out[0] = (uint64_t)n;
@@ -2026,10 +2136,15 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
              P.nblocks >= (int64_t)2 * want * kMinBlocksPerCta)
         want *= 2;
       // very few long rows leave most SMs idle even with a cluster per row:
-      // stream each row in kWideParts parts first
+      // stream each row in kWideParts parts first, or in twice as many when
+      // the SMs hold one part each
       if (want == kMaxSplit && (int64_t)cfg->rows * kMaxSplit * 4 <= (int64_t)sms &&
-          P.nblocks >= (int64_t)kWideParts * kMinBlocksPerCta)
+          P.nblocks >= (int64_t)kWideParts * kMinBlocksPerCta) {
         nparts = kWideParts;
+        if ((int64_t)cfg->rows * 2 * kWideParts <= (int64_t)sms &&
+            P.nblocks >= (int64_t)2 * kWideParts * kMinBlocksPerCta)
+          nparts = 2 * kWideParts;
+      }
     }
     for (split = want; split >= 1; split /= 2) {
       z = sizes_for(P, split);
@@ -2054,7 +2169,10 @@ int dsa_select_init(const dsa_select_cfg* cfg, int device, dsa_select_plan** pla
     }
   }
   // the wide split needs a cluster per row, and each cluster CTA's lists must
-  // fit its streaming buffer
+  // fit its streaming buffer (an automatic choice falls back to kWideParts)
+  if (cfg->split == 0 && nparts > kWideParts && split > 1 &&
+      ((int64_t)(nparts + split - 1) / split) * cfg->block_topk > z.cap)
+    nparts = kWideParts;
   if (split <= 1 || ((int64_t)(nparts + split - 1) / split) * cfg->block_topk > z.cap) nparts = 0;
   if (rc == DSA_OK && nparts > 0) {
     const size_t bytes = (size_t)cfg->rows * nparts * (cfg->block_topk + 1) * 8;

@@ -110,12 +110,12 @@ def test_ascending_values_force_many_compactions():
     check_all_modes(case, what="monotone")
 
 
-@pytest.mark.parametrize("split", [2, 4, 16, 32, 64])
+@pytest.mark.parametrize("split", [2, 4, 16, 32, 64, 128])
 @pytest.mark.parametrize("layout", ["aligned", "misaligned", "stride2", "b1"])
 def test_cluster_split_rows(split, layout):
     """k CTAs per row in a thread-block cluster: each streams a share of the
     blocks, the leader merges the shares over distributed shared memory.
-    split 32 / 64: the wide split -- the row streamed in that many parts by a
+    split 32 / 64 / 128: the wide split -- the row streamed in that many parts by a
     first launch, their top-Kb lists merged by a 16-CTA cluster."""
     rng = np.random.default_rng(split * 13 + len(layout))
     W, B, cs, starts = 200_000, 8, 1, [0, 4, 0, 100]
@@ -162,16 +162,20 @@ def test_auto_split_for_few_long_rows():
     assert few.describe()["split"] >= 8
     assert many.describe()["split"] == 1 and many.describe()["parts"] == 0
     # one 1M-column row leaves most SMs idle even with a 16-CTA cluster: the
-    # wide split streams it in 64 parts first
-    if few.describe()["sm_count"] >= 64 and few.describe()["split"] == 16:
-        assert few.describe()["parts"] == 64
+    # wide split streams it in 128 parts first (64 a row for two rows)
+    two = dsa.dsa_select_init(rows=2, width=1 << 20, block_size=8, block_topk=256, row_topk=2048)
+    sms = few.describe()["sm_count"]
+    if sms >= 128 and few.describe()["split"] == 16:
+        assert few.describe()["parts"] == 128
+    if sms >= 128 and two.describe()["split"] == 16:
+        assert two.describe()["parts"] == 64
 
 
 @pytest.mark.parametrize("rows", [1, 2])
 def test_one_or_two_1m_rows_auto_plan(rows):
     """P1's test plan: a single row over a 1M-column buffer -- in the plan the
-    device picks for it (on GB300 the wide split: 64 parts, then a 16-CTA
-    cluster per row), every column and index compared with the oracle in all
+    device picks for it (on GB300 the wide split: 128 parts for one row, 64
+    for two, then a 16-CTA cluster per row), every column and index compared with the oracle in all
     three modes.  The second row has a start, an end short of W and a spike
     mix; a third shape puts the pin past W."""
     W = 1 << 20
