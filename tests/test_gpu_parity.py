@@ -171,6 +171,24 @@ def test_auto_split_for_few_long_rows():
         assert two.describe()["parts"] == 64
 
 
+@pytest.mark.parametrize("split", [64, 128])
+def test_wide_split_large_kb(split):
+    """The wide split with Kb = 1000, K = 4096 on two 1M-column rows: a
+    cluster CTA's lists (8000 slots at 128 parts) are more than its threads
+    load in one round, and each part keeps up to 1000 of its 1024 or 2048
+    blocks."""
+    W = 1 << 20
+    rng = np.random.default_rng(300 + split)
+    x = rng.standard_normal((2, W)).astype(np.float32)
+    x[1, 500_000:520_000] = 7.0  # a run of equal maxima across parts
+    case = Case(x, [0, 40], [W, W - 12_345], width=W, block_size=8, block_topk=1000, row_topk=4096,
+                split=split)
+    desc = DeviceRun(case).plan.describe()
+    if desc["split"] == 16:  # a 16-CTA cluster of this shared memory fits on GB300
+        assert desc["parts"] == split
+    check_all_modes(case, what=f"wide split {split}, Kb 1000")
+
+
 @pytest.mark.parametrize("rows", [1, 2])
 def test_one_or_two_1m_rows_auto_plan(rows):
     """P1's test plan: a single row over a 1M-column buffer -- in the plan the
