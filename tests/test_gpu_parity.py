@@ -189,6 +189,38 @@ def test_wide_split_large_kb(split):
     check_all_modes(case, what=f"wide split {split}, Kb 1000")
 
 
+def test_wide_split_graph_replay():
+    """The wide split captured in a CUDA graph (the cluster launch is a
+    programmatic dependent of the parts' launch, an edge of the graph) and
+    replayed with new ends: a full row, a short one that leaves most parts
+    empty, one with the pin past W, one of five columns."""
+    import sparse_attention_indexer_live_gb300 as dsa
+    W = 1 << 20
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((1, W)).astype(np.float32)
+    x[0, rng.integers(0, W, 64)] = 6.0 + np.abs(rng.standard_normal(64)).astype(np.float32)
+    case = Case(x, None, [W], width=W, block_size=8, block_topk=256, row_topk=2048, split=128)
+    run = DeviceRun(case)
+    if run.plan.describe()["parts"] != 128:
+        pytest.skip("this device does not run the wide split")
+    base = run.buf.clone()
+    dsa.dsa_select_topk(run.plan, run.logits, None, run.ends, run.cand, run.topk)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        dsa.dsa_select_topk(run.plan, run.logits, None, run.ends, run.cand, run.topk, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    for replay in ([W], [300_001], [W + 5], [5], [W - 777]):
+        run.ends.copy_(torch.tensor(replay, dtype=torch.int32))
+        run.buf.copy_(base)
+        g.replay()
+        torch.cuda.synchronize()
+        c2 = Case(x, None, replay, width=W, block_size=8, block_topk=256, row_topk=2048)
+        assert_run_matches(run, *c2.oracle(), what=f"wide split replay {replay}")
+
+
 @pytest.mark.parametrize("rows", [1, 2])
 def test_one_or_two_1m_rows_auto_plan(rows):
     """P1's test plan: a single row over a 1M-column buffer -- in the plan the
