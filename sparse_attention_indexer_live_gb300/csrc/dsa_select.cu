@@ -101,7 +101,7 @@ struct Shared {
   uint32_t sel_above;
   uint32_t sel_count;
   int32_t counts[4];
-  int32_t part[kMaxSplit + 1];  // cluster leader: per-CTA counts, then offsets
+  int32_t part[2];              // cluster: [0] this CTA's offset in the leader's buffer, [1] the total
   int32_t kept_n;               // finish_block_topk: live kept ids left sorted in `keep`, or -1
   uint64_t tau;
 };
@@ -1315,11 +1315,13 @@ __device__ __noinline__ bool small_row(const Params& p, float* rowp, const Row& 
 //   buffer cap*8 and the candidate row top-k layout)
 //
 // kCluster: a thread-block cluster of k CTAs owns one row.  Each CTA streams
-// an equal share of the row's live blocks into its own top-Kb; the leader
-// (rank 0) merges the k lists through distributed shared memory, finishes the
-// block top-k and builds the bitmap; every CTA copies the bitmap words of its
-// share back and masks its share; the leader takes the row top-k.  Only the
-// cluster's hardware barriers order these steps.
+// an equal share of the row's live blocks (or, after a wide split's first
+// launch, loads its parts' lists) into its own top-Kb; every peer stores its
+// list into the leader's (rank 0) buffer through distributed shared memory;
+// the leader finishes the block top-k and builds the bitmap; the other CTAs
+// copy the bitmap words of their mask shares and mask the row while the
+// leader takes the row top-k.  Only the cluster's hardware barriers order
+// these steps.
 template <bool kTopK, bool kCluster>
 __global__ void __launch_bounds__(kThreads, 2) select_kernel(const Params p) {
   extern __shared__ __align__(16) uint8_t dyn[];
