@@ -142,11 +142,11 @@ struct Row {
   int32_t nb;   // live blocks
 };
 
-__device__ __forceinline__ Row load_row(const Params& p, int r) {
-  const int q = r / p.rep;
-  int64_t s = p.has_starts ? (int64_t)p.starts[q] : 0;
+// The row's bounds from the raw start and end of its group q = r / rep.
+__device__ __forceinline__ Row row_from(const Params& p, int r, int32_t start, int32_t end) {
+  int64_t s = start;
   if (s < 0) s = 0;
-  int64_t e = (int64_t)p.ends[q];
+  int64_t e = end;
   if (p.causal) e = e - (p.rep - 1) + (r % p.rep);
   int64_t ec = e < p.width ? e : p.width;
   Row R;
@@ -157,6 +157,11 @@ __device__ __forceinline__ Row load_row(const Params& p, int r) {
   R.L = (int32_t)L;
   R.nb = (int32_t)(L > 0 ? (L + p.B - 1) / p.B : 0);
   return R;
+}
+
+__device__ __forceinline__ Row load_row(const Params& p, int r) {
+  const int q = r / p.rep;
+  return row_from(p, r, p.has_starts ? p.starts[q] : 0, p.ends[q]);
 }
 
 // Exclusive block-wide prefix sum of one int per thread.  All threads call.
@@ -1828,50 +1833,79 @@ constexpr int kCombineThreads = 256;
 __global__ void __launch_bounds__(kCombineThreads) combine_window_kernel(const Params p, const int32_t* topk,
                                                                          int32_t window, int32_t* out) {
   extern __shared__ int32_t ts[];  // the row's top-k list, staged once (K entries)
-  __shared__ int s_cnt;
+  __shared__ int s_part[kCombineThreads / 32][3];
   const int r = blockIdx.x;
-  const Row R = load_row(p, r);
   const int K = p.K;
   const int32_t* gt = topk + (int64_t)r * K;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // The row's bounds and the first part of its list are read at once: the
+  // list's loads do not wait for the bounds.
+  const int q = r / p.rep;
+  const int32_t start = p.has_starts ? __ldg(p.starts + q) : 0;
+  const int32_t end = __ldg(p.ends + q);
+  const bool vec = (K & 3) == 0 && (reinterpret_cast<uintptr_t>(gt) & 15) == 0;
+  constexpr int kPre = 2;  // 16-byte loads of a thread issued before the bounds are used
+  int4 pre[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u) {
+    const int i = 4 * (int)threadIdx.x + 4 * kCombineThreads * u;
+    pre[u] = vec && i < K ? __ldg(reinterpret_cast<const int4*>(gt + i)) : make_int4(-1, -1, -1, -1);
+  }
+  const Row R = row_from(p, r, start, end);
   const int64_t width = (int64_t)K + window;
   int32_t* o = out + (int64_t)r * width;
   const int64_t w1 = R.s + R.L;
   const int64_t w0 = w1 - window > R.s ? w1 - window : R.s;
   const int nw = (int)(w1 - w0);
-  if (threadIdx.x == 0) s_cnt = 0;
-  // the list into shared memory in one pass (16-byte loads when aligned), so
-  // that the searches below do not wait on global memory step by step
-  int mine = 0;
-  if ((K & 3) == 0 && (reinterpret_cast<uintptr_t>(gt) & 15) == 0) {
-    for (int i = 4 * threadIdx.x; i < K; i += 4 * kCombineThreads) {
+  // the list into shared memory, counting its valid entries (an ascending
+  // prefix) and those below the window's start and end: their places follow
+  // from the counts, with no search
+  int c_valid = 0, c_w0 = 0, c_w1 = 0;
+  auto take = [&](int i, int32_t v) {
+    ts[i] = v;
+    c_valid += v >= 0;
+    c_w0 += v >= 0 && v < w0;
+    c_w1 += v >= 0 && v < w1;
+  };
+  if (vec) {
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int i = 4 * (int)threadIdx.x + 4 * kCombineThreads * u;
+      if (i < K) {
+        take(i, pre[u].x);
+        take(i + 1, pre[u].y);
+        take(i + 2, pre[u].z);
+        take(i + 3, pre[u].w);
+      }
+    }
+    for (int i = 4 * (int)threadIdx.x + 4 * kCombineThreads * kPre; i < K; i += 4 * kCombineThreads) {
       const int4 v = __ldg(reinterpret_cast<const int4*>(gt + i));
-      *reinterpret_cast<int4*>(ts + i) = v;
-      mine += (v.x >= 0) + (v.y >= 0) + (v.z >= 0) + (v.w >= 0);
+      take(i, v.x);
+      take(i + 1, v.y);
+      take(i + 2, v.z);
+      take(i + 3, v.w);
     }
   } else {
-    for (int i = threadIdx.x; i < K; i += kCombineThreads) {
-      const int32_t v = __ldg(gt + i);
-      ts[i] = v;
-      mine += v >= 0;
-    }
+    for (int i = threadIdx.x; i < K; i += kCombineThreads) take(i, __ldg(gt + i));
+  }
+  c_valid = __reduce_add_sync(kFull, c_valid);
+  c_w0 = __reduce_add_sync(kFull, c_w0);
+  c_w1 = __reduce_add_sync(kFull, c_w1);
+  if (lane == 0) {
+    s_part[warp][0] = c_valid;
+    s_part[warp][1] = c_w0;
+    s_part[warp][2] = c_w1;
   }
   __syncthreads();
-  atomicAdd(&s_cnt, mine);
-  __syncthreads();
+  int nt = 0, lb0 = 0, lb1 = 0;
+#pragma unroll
+  for (int w = 0; w < kCombineThreads / 32; ++w) {
+    nt += s_part[w][0];
+    lb0 += s_part[w][1];
+    lb1 += s_part[w][2];
+  }
+  const int absorbed = lb1 - lb0;  // top-k entries inside the window
   const int32_t* t = ts;
-  const int nt = s_cnt;  // valid entries: an ascending prefix of the list
-  int lo = 0, hi = nt;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (t[mid] < w0) lo = mid + 1; else hi = mid;
-  }
-  const int lb0 = lo;
-  hi = nt;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (t[mid] < w1) lo = mid + 1; else hi = mid;
-  }
-  const int absorbed = lo - lb0;  // top-k entries inside the window
   for (int i = threadIdx.x; i < nt; i += kCombineThreads) {
     const int64_t a = t[i];
     int64_t pos = -1;
